@@ -1,0 +1,158 @@
+/*
+ * fp4q.h - C ABI of the FP4 communication codec (compress, decompress-accumulate,
+ * fused roundtrip, emulated R-way reduce) for NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method:
+ *   [P1] "FP4Quant: Efficient 4-Bit Communication Compression for Model-Parallel LLM
+ *        Training" (shd-paper.top summary of arXiv 2611.04323), English abstract and the
+ *        method section's "technical framework" paragraph: micro-grouped dual-scale FP4
+ *        quantization, warp-cooperative FP4 packing, hybrid two-level FWHT.
+ *   [P3] "4-bit compression speeds up LLM training by 56 percent with minimal accuracy
+ *        loss" (zot.news), lead paragraph and "Read it as": small clusters of values share
+ *        scaling factors, values are packed two per byte, a fast transform keeps errors
+ *        low; the compressed tensors are the ones the tensor-parallel AllReduce exchanges.
+ *   [P4] "Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs"
+ *        (gist.science), technical summary, problem statement: FP4 elements are E2M1.
+ *
+ * The pages fix the shape of the method but none of its numbers. This header is the one
+ * place where the numbers are fixed; every kernel and the CPU oracle implement exactly
+ * this contract:
+ *
+ *   Block.   The tensor is cut into blocks of FP4Q_BLOCK = 256 consecutive elements.
+ *            n must be a positive multiple of 256 (no tail handling).
+ *   FWHT.    (fwht = 1) per block, y = (1/16) * H256 * x with H256 the Sylvester-ordered
+ *            Walsh-Hadamard matrix, H256 = H16 (x) H16. It is evaluated as the butterfly
+ *            sequence h = 1, 2, 4, ..., 128: for every j with (j & h) == 0,
+ *            (y[j], y[j+h]) <- (y[j] + y[j+h], y[j] - y[j+h]) in FP32 round-to-nearest,
+ *            then y <- y * 0.0625f. Stages h < 16 act inside a 16-element group (level 1),
+ *            stages h >= 16 act across the 16 groups of a block (level 2). [P1 "hybrid
+ *            two-level FWHT pipeline"; P3 "a fast transform keeps errors low"]
+ *   Scales.  Two levels [P1 "dual-scale"; P3 "tiny clusters of values share scaling
+ *            factors"]:
+ *              A_b = max |y| over the block.
+ *              If A_b < 2688 * 2^-100 the block is all-zero: s_b = 0, every group scale
+ *              byte 0x00, every code 0x0.
+ *              Otherwise s_b = A_b / 2688.0f   (2688 = 6 * 448, FP32 IEEE division).
+ *              t_b = s_b * 6.0f; per group of G elements r_g = amax_g / t_b (IEEE div);
+ *              s_g = E4M3(r_g): round to nearest, ties to the even code, saturating at
+ *              448 (OCP e4m3fn, codes 0x00..0x7E, never 0x7F).
+ *   Codes.   S_g = float(s_g) * s_b; inv_g = S_g > 0 ? 1.0f / S_g : 0.0f (IEEE);
+ *            q = y * inv_g; code = sign(q) << 3 | E2M1(|q|), E2M1 = round to nearest,
+ *            ties to the even code, onto {0, 0.5, 1, 1.5, 2, 3, 4, 6} (codes 0..7),
+ *            saturating at 6. The sign is kept: a negative q that rounds to 0 gives 0x8.
+ *            [P4 "E2M1"; P1 "FP4"]
+ *   Packing. byte k of the code segment = code[2k] | code[2k+1] << 4 (even element in
+ *            the low nibble). [P3 "packed two per byte"]
+ *   Payload. One contiguous byte buffer, structure of arrays:
+ *              [codes: n/2 bytes][group scales: n/G bytes, zero-padded to a multiple of
+ *              16][block scales: n/256 x float32, little endian]
+ *            Every segment starts 16-byte aligned when the buffer does. A contiguous range
+ *            of blocks can be cut out of each segment.
+ *   Decode.  x~ = grid(code) * S_g (signed, FP32); if fwht, the same butterfly sequence
+ *            h = 1..128 followed by * 0.0625f (H is symmetric and H*H = I).
+ *   Reduce.  z = x~_0 + x~_1 + ... + x~_{R-1} (FP32, in rank order, no FMA), decoded in
+ *            the transform domain (no inverse FWHT), then Scales/Codes/Packing on z with
+ *            no forward FWHT. [P3 "Read it as": the AllReduce of tensor parallelism]
+ *
+ * Every floating-point step is a separately rounded FP32 operation (no FMA contraction),
+ * so the GPU result is bit-identical to a plain scalar evaluation of the steps above.
+ *
+ * Preconditions on data (not checked): inputs finite and |x| < 2^120.
+ *
+ * Threading and ownership: the caller owns every buffer; the library keeps no per-call
+ * state and allocates no device memory. All entry points are asynchronous on the given
+ * stream and never synchronise. Argument errors are returned before anything is launched.
+ * A failed launch returns FP4Q_ERR_CUDA (the CUDA error is left to the caller's next
+ * runtime call to report).
+ */
+#ifndef FP4Q_H
+#define FP4Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP4Q_BLOCK 256              /* elements per block (FWHT length, block scale)   */
+#define FP4Q_GROUP_DEFAULT 16       /* elements per micro-group (E4M3 scale)           */
+#define FP4Q_MAX_RANKS 8            /* largest R accepted by fp4q_reduce_requantize    */
+#define FP4Q_E4M3_MAX 448.0f        /* largest finite e4m3fn value                      */
+#define FP4Q_E2M1_MAX 6.0f          /* largest E2M1 value                               */
+#define FP4Q_BLOCK_DENOM 2688.0f    /* FP4Q_E4M3_MAX * FP4Q_E2M1_MAX                    */
+
+typedef enum fp4q_status {
+  FP4Q_OK = 0,
+  FP4Q_ERR_NULL = 1,     /* a required pointer is NULL                                  */
+  FP4Q_ERR_SIZE = 2,     /* n <= 0, n % 256 != 0, or n >= 2^40                          */
+  FP4Q_ERR_ALIGN = 3,    /* a data pointer is not 16-byte aligned                       */
+  FP4Q_ERR_PARAM = 4,    /* bad params: group not 16/32, block not 256, fwht not 0/1,
+                            R outside [1, 8], unknown dtype, beta not 0/1               */
+  FP4Q_ERR_OVERLAP = 5,  /* an output buffer overlaps an input buffer                   */
+  FP4Q_ERR_CUDA = 6      /* a CUDA runtime call or a kernel launch failed               */
+} fp4q_status;
+
+typedef struct fp4q_params {
+  int32_t group;  /* G: 16 (default) or 32 elements per group scale                    */
+  int32_t block;  /* must be 256                                                        */
+  int32_t fwht;   /* 1: apply the FWHT (default); 0: quantize the raw values            */
+} fp4q_params;
+
+typedef enum fp4q_dtype {
+  FP4Q_BF16 = 0,  /* destination is bfloat16, rounded to nearest even                   */
+  FP4Q_F32 = 1    /* destination is float32                                             */
+} fp4q_dtype;
+
+/* Bytes of the payload for n elements: n/2 + pad16(n/G) + 4*(n/256).
+ * Returns 0 when n or params are invalid. params == NULL means the defaults {16,256,1}. */
+size_t fp4q_payload_bytes(int64_t n, const fp4q_params* params);
+
+/* Byte offsets of the group-scale and block-scale segments inside the payload
+ * (the code segment starts at offset 0). Return 0 on invalid arguments. */
+size_t fp4q_gscale_offset(int64_t n, const fp4q_params* params);
+size_t fp4q_bscale_offset(int64_t n, const fp4q_params* params);
+
+/* Compress: x_bf16 (device, n bfloat16, 16-byte aligned) -> payload (device,
+ * fp4q_payload_bytes(n) bytes, 16-byte aligned). Steps FWHT, Scales, Codes, Packing
+ * above [P1 abstract: micro-grouped dual-scale FP4 quantization, warp-cooperative
+ * packing, two-level FWHT]. payload must not overlap x (FP4Q_ERR_OVERLAP).
+ * stream: a cudaStream_t (NULL = legacy default stream). */
+fp4q_status fp4q_compress(const void* x_bf16, int64_t n, void* payload,
+                          const fp4q_params* params, void* stream);
+
+/* Decompress-accumulate: payload (device) -> dst (device, n elements of dtype, 16-byte
+ * aligned). dst = beta ? dst + x^ : x^, where x^ is the Decode step above; for a bfloat16
+ * dst the sum is formed in FP32 and rounded to nearest even once. This is the receive side
+ * of the compressed AllReduce [P3 "Read it as"]. dst may not overlap payload. */
+fp4q_status fp4q_decompress_accumulate(const void* payload, int64_t n, void* dst,
+                                       fp4q_dtype dtype, int32_t beta,
+                                       const fp4q_params* params, void* stream);
+
+/* Fused roundtrip (fake quantization): y_bf16 = bf16(decode(compress(x_bf16))) without
+ * writing a payload. Bit-identical to fp4q_compress followed by
+ * fp4q_decompress_accumulate(..., FP4Q_BF16, beta = 0). y must not overlap x. */
+fp4q_status fp4q_roundtrip(const void* x_bf16, int64_t n, void* y_bf16,
+                           const fp4q_params* params, void* stream);
+
+/* Emulated R-way reduce: payloads is a HOST array of R device pointers, each a payload of
+ * n elements made with the same params; out_payload (device) receives the requantized sum
+ * (Reduce step above). This is the fused decompress-sum-requantize step of a
+ * reduce-scatter/all-gather AllReduce with all R rank buffers resident on one GPU
+ * [P3 "Read it as"]. params->fwht only records the domain of the payloads; the reduce never
+ * transforms. out_payload may not overlap any input payload. 1 <= R <= FP4Q_MAX_RANKS. */
+fp4q_status fp4q_reduce_requantize(const void* const* payloads, int32_t R, int64_t n,
+                                   void* out_payload, const fp4q_params* params,
+                                   void* stream);
+
+/* Static string naming a status code (never NULL). */
+const char* fp4q_status_string(fp4q_status status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int32_t fp4q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4Q_H */
