@@ -48,8 +48,10 @@
  *              16][block scales: n/256 x float32, little endian]
  *            Every segment starts 16-byte aligned when the buffer does. A contiguous range
  *            of blocks can be cut out of each segment.
- *   Decode.  x~ = grid(code) * S_g (signed, FP32); if fwht, the same butterfly sequence
- *            h = 1..128 followed by * 0.0625f (H is symmetric and H*H = I).
+ *   Decode.  x~ = grid(code) * S_g (signed, FP32); if fwht, the inverse transform: the
+ *            same butterflies in mirror order h = 128, 64, ..., 1 (level 2, then level 1),
+ *            followed by * 0.0625f (H is symmetric and H*H = I, so the stages of the forward
+ *            transform undone in reverse order give the inverse).
  *   Reduce.  z = x~_0 + x~_1 + ... + x~_{R-1} (FP32, in rank order, no FMA), decoded in
  *            the transform domain (no inverse FWHT), then Scales/Codes/Packing on z with
  *            no forward FWHT. [P3 "Read it as": the AllReduce of tensor parallelism]

@@ -65,7 +65,8 @@ def _load():
             "oracle_e4m3_encode_array": (None, [P, P, I64]),
             "oracle_e2m1_encode_array": (None, [P, P, I64]),
             "oracle_bf16_round_array": (None, [P, P, I64]),
-            "oracle_fwht256_array": (None, [P, I64]),
+            "oracle_fwht256_array": (None, [P, I64, I]),
+            "oracle_ifwht256": (None, [P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -130,11 +131,12 @@ def bf16_to_f32(h) -> np.ndarray:
     return (h.astype(np.uint32) << 16).view(np.float32)
 
 
-def fwht256(v) -> np.ndarray:
-    """Orthonormal FWHT of each consecutive 256-block of v (float32); returns a copy."""
+def fwht256(v, inverse: bool = False) -> np.ndarray:
+    """Orthonormal FWHT of each consecutive 256-block of v (float32); returns a copy.
+    inverse=True applies the decode's mirror stage order (h = 128 ... 1)."""
     v = np.array(v, dtype=np.float32, copy=True).ravel()
     assert v.size % BLOCK == 0
-    _load().oracle_fwht256_array(_ptr(v), v.size // BLOCK)
+    _load().oracle_fwht256_array(_ptr(v), v.size // BLOCK, int(bool(inverse)))
     return v
 
 

@@ -124,9 +124,25 @@ uint8_t oracle_e2m1_encode(float q) {
  * FP32, then a multiplication by 1/16. Strides below 16 mix the elements of one 16-element
  * group (level 1); strides of 16 and more mix the 16 groups (level 2), i.e.
  * H256 = H16 (x) H16. [P1 "hybrid two-level FWHT pipeline"; P3 "a fast transform"]
- * H is symmetric and H * H = I, so the same routine is its own inverse. */
+ * This is the forward transform of compress. */
 void oracle_fwht256(float* v) {
   for (int h = 1; h < ORACLE_BLOCK; h <<= 1) {
+    for (int j = 0; j < ORACLE_BLOCK; ++j) {
+      if (j & h) continue;
+      float a = v[j], b = v[j + h];
+      v[j] = a + b;
+      v[j + h] = a - b;
+    }
+  }
+  for (int j = 0; j < ORACLE_BLOCK; ++j) v[j] = v[j] * 0.0625f;
+}
+
+/* Inverse transform used by every decode: the same butterflies in mirror order
+ * (h = 128, 64, ..., 1: level 2 across groups first, then level 1 inside each group),
+ * then a multiplication by 1/16. In exact arithmetic this equals oracle_fwht256 (the stages
+ * commute and H * H = I); the order is fixed because FP32 rounding depends on it. */
+void oracle_ifwht256(float* v) {
+  for (int h = ORACLE_BLOCK / 2; h >= 1; h >>= 1) {
     for (int j = 0; j < ORACLE_BLOCK; ++j) {
       if (j & h) continue;
       float a = v[j], b = v[j + h];
@@ -263,8 +279,8 @@ int oracle_compress(const uint16_t* x, int64_t n, uint8_t* payload, int G, int f
   return 0;
 }
 
-/* Decode every block of a payload to FP32 in the original domain (inverse FWHT if fwht).
- * out has n floats. */
+/* Decode block b of a payload to 256 FP32 values: x~ = grid(code) * S, then the inverse
+ * FWHT (mirror stage order) when fwht is set. */
 static void decode_all(const uint8_t* payload, int64_t n, int G, int fwht, int64_t b,
                        float* xh) {
   const uint8_t* codes = payload;
@@ -273,7 +289,7 @@ static void decode_all(const uint8_t* payload, int64_t n, int G, int fwht, int64
   float s_b;
   memcpy(&s_b, bsc + 4 * b, 4);
   dequantize_block(codes + b * (ORACLE_BLOCK / 2), gsc + b * (ORACLE_BLOCK / G), s_b, G, xh);
-  if (fwht) oracle_fwht256(xh);
+  if (fwht) oracle_ifwht256(xh);
 }
 
 /* Decompress-accumulate: dst = beta ? dst + x^ : x^ (dtype 0: bfloat16 dst, the sum formed
@@ -365,8 +381,12 @@ void oracle_bf16_round_array(const float* f, uint16_t* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(f[i]);
 }
 
-/* FWHT of nblk consecutive 256-element blocks, in place. */
-void oracle_fwht256_array(float* v, int64_t nblk) {
+/* Forward (inverse = 0) or inverse (inverse = 1) FWHT of nblk consecutive 256-element
+ * blocks, in place. */
+void oracle_fwht256_array(float* v, int64_t nblk, int inverse) {
 #pragma omp parallel for schedule(static)
-  for (int64_t b = 0; b < nblk; ++b) oracle_fwht256(v + b * ORACLE_BLOCK);
+  for (int64_t b = 0; b < nblk; ++b) {
+    if (inverse) oracle_ifwht256(v + b * ORACLE_BLOCK);
+    else oracle_fwht256(v + b * ORACLE_BLOCK);
+  }
 }

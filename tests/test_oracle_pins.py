@@ -42,33 +42,45 @@ def _blocks(seed, k):
     return x
 
 
-def test_fwht_matches_dense_fp64_hadamard():
-    """Butterfly FWHT in FP32 vs the dense product H256 x / 16 in FP64 (scipy's Hadamard).
-    Error bound of 8 stages of RN butterflies on an orthogonal transform: 8 u ||x||."""
+@pytest.mark.parametrize("inverse", [False, True])
+def test_fwht_matches_dense_fp64_hadamard(inverse):
+    """Butterfly FWHT in FP32 (forward order, and the decode's mirror order) vs the dense
+    product H256 x / 16 in FP64 (scipy's Hadamard). Error bound of 8 stages of RN
+    butterflies on an orthogonal transform: 8 u ||x||."""
     x = _blocks(1, 64)
-    y = oracle.fwht256(x).reshape(x.shape).astype(np.float64)
+    y = oracle.fwht256(x, inverse).reshape(x.shape).astype(np.float64)
     exact = x.astype(np.float64) @ H256.T / 16.0
     for i in range(x.shape[0]):
         nx = np.linalg.norm(x[i].astype(np.float64))
         assert np.linalg.norm(y[i] - exact[i]) <= 8 * U * nx * (1 + 1e-9)
 
 
-def test_fwht_special_cases_exact():
+def test_forward_and_mirror_orders_round_differently():
+    """The two stage orders agree in exact arithmetic but not bit for bit, which is why the
+    decode's order is part of the contract."""
+    x = _blocks(9, 64)
+    a, b = oracle.fwht256(x), oracle.fwht256(x, inverse=True)
+    assert not np.array_equal(a, b)
+    assert np.max(np.abs(a - b)) <= 1e-5 * np.max(np.abs(a))
+
+
+@pytest.mark.parametrize("inverse", [False, True])
+def test_fwht_special_cases_exact(inverse):
     e0 = np.zeros(256, np.float32); e0[0] = 1
-    assert np.array_equal(oracle.fwht256(e0), np.full(256, 0.0625, np.float32))
+    assert np.array_equal(oracle.fwht256(e0, inverse), np.full(256, 0.0625, np.float32))
     for k in (1, 2, 17, 128, 255):
         ek = np.zeros(256, np.float32); ek[k] = 1
         expect = np.array([(-1) ** bin(i & k).count("1") / 16 for i in range(256)], np.float32)
-        assert np.array_equal(oracle.fwht256(ek), expect)
+        assert np.array_equal(oracle.fwht256(ek, inverse), expect)
     ones = np.ones(256, np.float32)
     expect = np.zeros(256, np.float32); expect[0] = 16
-    assert np.array_equal(oracle.fwht256(ones), expect)
+    assert np.array_equal(oracle.fwht256(ones, inverse), expect)
 
 
 def test_fwht_is_an_involution_and_preserves_energy():
     x = _blocks(2, 32)
     y = oracle.fwht256(x).reshape(x.shape)
-    z = oracle.fwht256(y).reshape(x.shape)
+    z = oracle.fwht256(y, inverse=True).reshape(x.shape)
     for i in range(x.shape[0]):
         nx = np.linalg.norm(x[i].astype(np.float64))
         assert np.linalg.norm(z[i].astype(np.float64) - x[i]) <= 16 * U * nx
@@ -81,11 +93,13 @@ def test_fwht_levels_act_on_groups_then_across_groups():
     position only excites group 0 (level 2)."""
     rng = np.random.default_rng(3)
     g = np.repeat(rng.integers(-8, 8, 16).astype(np.float32), 16)       # const per group
-    y = oracle.fwht256(g)
-    assert np.all(y.reshape(16, 16)[:, 1:] == 0)
+    for inv in (False, True):
+        y = oracle.fwht256(g, inv)
+        assert np.all(y.reshape(16, 16)[:, 1:] == 0)
     p = np.tile(rng.integers(-8, 8, 16).astype(np.float32), 16)          # same in every group
-    y = oracle.fwht256(p)
-    assert np.all(y.reshape(16, 16)[1:, :] == 0)
+    for inv in (False, True):
+        y = oracle.fwht256(p, inv)
+        assert np.all(y.reshape(16, 16)[1:, :] == 0)
 
 
 # ---------------------------------------------------------------------------- rounding
