@@ -1,0 +1,128 @@
+"""GB300-native FP4 communication compression (FP4Quant's data-parallel hot path).
+
+Torch-facing wrappers of the C ABI in ``include/fp4q.h``; the names follow the ABI. Every
+function takes CUDA tensors, runs on the current torch stream (or the ``stream`` given)
+and returns without synchronising. The codec itself runs only in the sm_103a kernels of
+``csrc/fp4q.cu``; there is no CPU fallback (a missing library raises ``RuntimeError``).
+
+    payload = compress(x)                                  # x: bfloat16, numel % 256 == 0
+    decompress_accumulate(payload, x.numel(), dst, beta=1) # dst += decode(payload)
+    y = roundtrip(x)                                       # fused fake-quantisation
+    out = reduce_requantize([p0, p1, p2, p3], n)           # emulated 4-rank reduce
+
+Method: "FP4Quant: Efficient 4-Bit Communication Compression for Model-Parallel LLM
+Training" (abstract: micro-grouped dual-scale FP4 quantization, warp-cooperative FP4
+packing, hybrid two-level FWHT).
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import BF16, F32, Fp4qError, build  # noqa: F401
+
+__all__ = ["payload_bytes", "gscale_offset", "bscale_offset", "compress",
+           "decompress_accumulate", "roundtrip", "reduce_requantize", "build", "Fp4qError",
+           "library_path"]
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _stream(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def payload_bytes(n: int, group: int = 16, fwht: int = 1) -> int:
+    p = _lib.params(group, fwht)
+    return int(_lib.lib().fp4q_payload_bytes(int(n), ctypes.byref(p)))
+
+
+def gscale_offset(n: int, group: int = 16, fwht: int = 1) -> int:
+    p = _lib.params(group, fwht)
+    return int(_lib.lib().fp4q_gscale_offset(int(n), ctypes.byref(p)))
+
+
+def bscale_offset(n: int, group: int = 16, fwht: int = 1) -> int:
+    p = _lib.params(group, fwht)
+    return int(_lib.lib().fp4q_bscale_offset(int(n), ctypes.byref(p)))
+
+
+def compress(x, payload=None, group: int = 16, fwht: int = 1, stream=None):
+    """bfloat16 CUDA tensor -> uint8 payload tensor (allocated by torch if not given)."""
+    import torch
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    n = x.numel()
+    if payload is None:
+        nb = payload_bytes(n, group, fwht)
+        if nb == 0:
+            raise ValueError(f"invalid size {n} (must be a positive multiple of 256)")
+        payload = torch.empty(nb, dtype=torch.uint8, device=x.device)
+    p = _lib.params(group, fwht)
+    st = _lib.lib().fp4q_compress(_dev(x, "x"), n, _dev(payload, "payload"), ctypes.byref(p),
+                                  _stream(stream, x.device))
+    _lib.check("fp4q_compress", st)
+    return payload
+
+
+def decompress_accumulate(payload, n: int, dst, beta: int = 1, group: int = 16, fwht: int = 1,
+                          stream=None):
+    """dst (bfloat16 or float32 CUDA tensor of n elements) = beta ? dst + x^ : x^."""
+    import torch
+    if dst.dtype == torch.bfloat16:
+        dt = BF16
+    elif dst.dtype == torch.float32:
+        dt = F32
+    else:
+        raise TypeError("dst must be bfloat16 or float32")
+    if dst.numel() != n:
+        raise ValueError("dst must have n elements")
+    p = _lib.params(group, fwht)
+    st = _lib.lib().fp4q_decompress_accumulate(_dev(payload, "payload"), int(n), _dev(dst, "dst"),
+                                               dt, int(beta), ctypes.byref(p),
+                                               _stream(stream, dst.device))
+    _lib.check("fp4q_decompress_accumulate", st)
+    return dst
+
+
+def roundtrip(x, y=None, group: int = 16, fwht: int = 1, stream=None):
+    """y = bf16(decode(compress(x))) in one kernel, no payload written."""
+    import torch
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    if y is None:
+        y = torch.empty_like(x)
+    p = _lib.params(group, fwht)
+    st = _lib.lib().fp4q_roundtrip(_dev(x, "x"), x.numel(), _dev(y, "y"), ctypes.byref(p),
+                                   _stream(stream, x.device))
+    _lib.check("fp4q_roundtrip", st)
+    return y
+
+
+def reduce_requantize(payloads, n: int, out=None, group: int = 16, fwht: int = 1, stream=None):
+    """R payloads (uint8 CUDA tensors, same n and params) -> requantised sum payload."""
+    import torch
+    R = len(payloads)
+    ptrs = (ctypes.c_void_p * max(R, 1))(*[_dev(p, "payload").value for p in payloads])
+    if out is None:
+        out = torch.empty(payload_bytes(n, group, fwht), dtype=torch.uint8,
+                          device=payloads[0].device)
+    p = _lib.params(group, fwht)
+    st = _lib.lib().fp4q_reduce_requantize(ctypes.cast(ptrs, ctypes.c_void_p), R, int(n),
+                                           _dev(out, "out"), ctypes.byref(p),
+                                           _stream(stream, out.device))
+    _lib.check("fp4q_reduce_requantize", st)
+    return out

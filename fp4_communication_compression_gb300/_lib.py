@@ -1,0 +1,104 @@
+"""ctypes binding of the fp4q C ABI (include/fp4q.h): argument marshalling only.
+
+Every step of the codec runs in the CUDA kernels of ``csrc/fp4q.cu``; this module only
+turns torch tensors into device pointers and the current torch stream into a
+``cudaStream_t``. There is no CPU path: if the library has not been built, every call
+raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+_SRC = os.path.join(_PKG, "csrc", "fp4q.cu")
+_HDR = os.path.join(_ROOT, "include", "fp4q.h")
+LIB_PATH = os.path.join(_PKG, f"libfp4q_{platform.machine()}.so")
+
+NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-fmad=false",
+              "-std=c++17", "-Xcompiler", "-fPIC", "-shared"]
+
+# status codes (fp4q_status)
+OK, ERR_NULL, ERR_SIZE, ERR_ALIGN, ERR_PARAM, ERR_OVERLAP, ERR_CUDA = range(7)
+BF16, F32 = 0, 1
+
+# exported symbols of the library, in the order include/fp4q.h declares them
+EXPORTS = ["fp4q_payload_bytes", "fp4q_gscale_offset", "fp4q_bscale_offset", "fp4q_compress",
+           "fp4q_decompress_accumulate", "fp4q_roundtrip", "fp4q_reduce_requantize",
+           "fp4q_status_string", "fp4q_version"]
+
+
+class Fp4qError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("group", ctypes.c_int32), ("block", ctypes.c_int32), ("fwht", ctypes.c_int32)]
+
+
+def build(force: bool = False, nvcc: str = "nvcc") -> str:
+    """Compile csrc/fp4q.cu for sm_103a into the package directory; returns the .so path."""
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
+        return LIB_PATH
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    cmd = [nvcc, *NVCC_FLAGS, "-I", os.path.dirname(_HDR), _SRC, "-o", tmp]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """The loaded library (raises RuntimeError if it was never built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"fp4q CUDA library not built ({LIB_PATH} missing); "
+                               "run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        pp = ctypes.POINTER(Params)
+        sig = {
+            "fp4q_payload_bytes": (SZ, [I64, pp]),
+            "fp4q_gscale_offset": (SZ, [I64, pp]),
+            "fp4q_bscale_offset": (SZ, [I64, pp]),
+            "fp4q_compress": (ctypes.c_int, [P, I64, P, pp, P]),
+            "fp4q_decompress_accumulate": (ctypes.c_int, [P, I64, P, ctypes.c_int, I32, pp, P]),
+            "fp4q_roundtrip": (ctypes.c_int, [P, I64, P, pp, P]),
+            "fp4q_reduce_requantize": (ctypes.c_int, [P, I32, I64, P, pp, P]),
+            "fp4q_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "fp4q_version": (I32, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+        return L
+
+
+def params(group: int = 16, fwht: int = 1, block: int = 256) -> Params:
+    return Params(group, block, fwht)
+
+
+def status_string(status: int) -> str:
+    return lib().fp4q_status_string(status).decode()
+
+
+def check(fn: str, status: int) -> None:
+    if status != OK:
+        raise Fp4qError(fn, status, status_string(status))

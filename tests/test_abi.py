@@ -1,0 +1,136 @@
+"""C ABI checks that need no GPU: the library builds, loads and exports every function
+include/fp4q.h declares; sizes and offsets follow the payload layout; and every argument
+error is returned as a status before anything is launched (each call below fails a host
+check, so no CUDA call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from fp4_communication_compression_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp4q.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _lib.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp4q_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert L.fp4q_version() >= 100
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert isinstance(_lib.status_string(s), str) and _lib.status_string(s)
+    assert _lib.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("n", [256, 4096, 256 * 17, 1 << 24, 256 * 1001])
+@pytest.mark.parametrize("G", [16, 32])
+def test_payload_layout_matches_oracle(L, n, G):
+    p = _lib.params(G, 1)
+    assert L.fp4q_payload_bytes(n, ctypes.byref(p)) == oracle.payload_bytes(n, G)
+    assert L.fp4q_gscale_offset(n, ctypes.byref(p)) == oracle.gscale_offset(n, G)
+    assert L.fp4q_bscale_offset(n, ctypes.byref(p)) == oracle.bscale_offset(n, G)
+    assert L.fp4q_bscale_offset(n, ctypes.byref(p)) % 16 == 0
+
+
+def test_payload_bytes_defaults_and_invalid(L):
+    assert L.fp4q_payload_bytes(4096, None) == 2368
+    for n in (0, -256, 100, 1 << 40):
+        assert L.fp4q_payload_bytes(n, None) == 0
+    for g, b, f in [(8, 256, 1), (16, 128, 1), (16, 256, 2), (64, 256, 0)]:
+        assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(g, b, f))) == 0
+
+
+# Fake, never dereferenced device addresses: every call below must fail a host check.
+A = 0x7f0000000000          # 16-byte aligned
+B = 0x7f0000100000
+P = _lib.params(16, 1)
+
+
+def test_compress_argument_errors(L):
+    pp = ctypes.byref(P)
+    assert L.fp4q_compress(None, 4096, B, pp, None) == _lib.ERR_NULL
+    assert L.fp4q_compress(A, 4096, None, pp, None) == _lib.ERR_NULL
+    for n in (0, -256, 100, 4095, 1 << 40):
+        assert L.fp4q_compress(A, n, B, pp, None) == _lib.ERR_SIZE
+    assert L.fp4q_compress(A + 8, 4096, B, pp, None) == _lib.ERR_ALIGN
+    assert L.fp4q_compress(A, 4096, B + 2, pp, None) == _lib.ERR_ALIGN
+    assert L.fp4q_compress(A, 4096, A + 16, pp, None) == _lib.ERR_OVERLAP
+    assert L.fp4q_compress(A, 4096, A + 2 * 4096 - 16, pp, None) == _lib.ERR_OVERLAP
+    for bad in [(8, 256, 1), (16, 512, 1), (16, 256, -1), (33, 256, 0)]:
+        assert L.fp4q_compress(A, 4096, B, ctypes.byref(_lib.Params(*bad)), None) == _lib.ERR_PARAM
+
+
+def test_decompress_argument_errors(L):
+    pp = ctypes.byref(P)
+    f = L.fp4q_decompress_accumulate
+    assert f(None, 4096, B, _lib.BF16, 1, pp, None) == _lib.ERR_NULL
+    assert f(A, 4096, None, _lib.BF16, 1, pp, None) == _lib.ERR_NULL
+    assert f(A, 4096, B, 2, 1, pp, None) == _lib.ERR_PARAM
+    assert f(A, 4096, B, _lib.BF16, 2, pp, None) == _lib.ERR_PARAM
+    assert f(A, 4096, B, _lib.F32, -1, pp, None) == _lib.ERR_PARAM
+    assert f(A, 300, B, _lib.BF16, 1, pp, None) == _lib.ERR_SIZE
+    assert f(A + 4, 4096, B, _lib.BF16, 1, pp, None) == _lib.ERR_ALIGN
+    assert f(A, 4096, B + 4, _lib.F32, 0, pp, None) == _lib.ERR_ALIGN
+    assert f(A, 4096, A + 2048, _lib.BF16, 1, pp, None) == _lib.ERR_OVERLAP
+    # a float32 dst is twice as long as a bfloat16 one: overlap is checked on its real size
+    assert f(A + 8192 + 16, 4096, A, _lib.F32, 1, pp, None) == _lib.ERR_OVERLAP
+
+
+def test_roundtrip_argument_errors(L):
+    pp = ctypes.byref(P)
+    f = L.fp4q_roundtrip
+    assert f(None, 4096, B, pp, None) == _lib.ERR_NULL
+    assert f(A, 4096, None, pp, None) == _lib.ERR_NULL
+    assert f(A, 257, B, pp, None) == _lib.ERR_SIZE
+    assert f(A, 4096, B + 8, pp, None) == _lib.ERR_ALIGN
+    assert f(A, 4096, A, pp, None) == _lib.ERR_OVERLAP
+    assert f(A, 4096, A + 8176, pp, None) == _lib.ERR_OVERLAP
+
+
+def test_reduce_argument_errors(L):
+    pp = ctypes.byref(P)
+    f = L.fp4q_reduce_requantize
+
+    def arr(*ptrs):
+        a = (ctypes.c_void_p * len(ptrs))(*ptrs)
+        return ctypes.cast(a, ctypes.c_void_p)
+
+    two = arr(A, A + 0x10000)
+    assert f(two, 0, 4096, B, pp, None) == _lib.ERR_PARAM
+    assert f(two, 9, 4096, B, pp, None) == _lib.ERR_PARAM
+    assert f(None, 2, 4096, B, pp, None) == _lib.ERR_NULL
+    assert f(two, 2, 4096, None, pp, None) == _lib.ERR_NULL
+    assert f(arr(A, None), 2, 4096, B, pp, None) == _lib.ERR_NULL
+    assert f(two, 2, 1000, B, pp, None) == _lib.ERR_SIZE
+    assert f(arr(A, A + 0x10008), 2, 4096, B, pp, None) == _lib.ERR_ALIGN
+    assert f(two, 2, 4096, B + 4, pp, None) == _lib.ERR_ALIGN
+    assert f(two, 2, 4096, A + 0x10000 + 1024, pp, None) == _lib.ERR_OVERLAP
+    assert f(two, 2, 4096, A, pp, None) == _lib.ERR_OVERLAP
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.lib()
