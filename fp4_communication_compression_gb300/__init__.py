@@ -23,7 +23,7 @@ from ._lib import BF16, F32, Fp4qError, build  # noqa: F401
 
 __all__ = ["payload_bytes", "gscale_offset", "bscale_offset", "compress",
            "decompress_accumulate", "roundtrip", "reduce_requantize", "build", "Fp4qError",
-           "library_path"]
+           "library_path", "fault_flags"]
 
 
 def library_path() -> str:
@@ -126,3 +126,10 @@ def reduce_requantize(payloads, n: int, out=None, group: int = 16, fwht: int = 1
                                            _stream(stream, out.device))
     _lib.check("fp4q_reduce_requantize", st)
     return out
+
+
+def fault_flags(clear: bool = False) -> int:
+    """The device fault word (0 = every bounded wait completed); synchronises the device."""
+    v = ctypes.c_uint32(0)
+    _lib.check("fp4q_fault_flags", _lib.lib().fp4q_fault_flags(ctypes.byref(v), int(bool(clear))))
+    return int(v.value)

@@ -29,7 +29,7 @@ BF16, F32 = 0, 1
 # exported symbols of the library, in the order include/fp4q.h declares them
 EXPORTS = ["fp4q_payload_bytes", "fp4q_gscale_offset", "fp4q_bscale_offset", "fp4q_compress",
            "fp4q_decompress_accumulate", "fp4q_roundtrip", "fp4q_reduce_requantize",
-           "fp4q_status_string", "fp4q_version"]
+           "fp4q_fault_flags", "fp4q_selftest_wait_timeout", "fp4q_status_string", "fp4q_version"]
 
 
 class Fp4qError(RuntimeError):
@@ -80,6 +80,8 @@ def lib():
             "fp4q_decompress_accumulate": (ctypes.c_int, [P, I64, P, ctypes.c_int, I32, pp, P]),
             "fp4q_roundtrip": (ctypes.c_int, [P, I64, P, pp, P]),
             "fp4q_reduce_requantize": (ctypes.c_int, [P, I32, I64, P, pp, P]),
+            "fp4q_fault_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), I32]),
+            "fp4q_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, P]),
             "fp4q_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "fp4q_version": (I32, []),
         }

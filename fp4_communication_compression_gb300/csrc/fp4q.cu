@@ -29,6 +29,7 @@
 //     with the sign of z either way);
 //   * all E2M1 / E4M3 rounding is done by the sm_100-family cvt instructions, which round
 //     to nearest even with saturation exactly as the contract states.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -38,12 +39,9 @@
 
 namespace {
 
-constexpr int kBlock = 256;
 constexpr int kTileBlocks = 8;                  // 256-element blocks per warp tile
-constexpr int kCtaWarps = 8;                    // warps per CTA
+constexpr int kCtaWarps = 4;                    // warps per CTA
 constexpr int kUnitsPerBlock = 73;              // 16-byte units per block in the transpose buffer
-constexpr int kWarpSmemBytes = kTileBlocks * kUnitsPerBlock * 16;
-constexpr int kCtaSmemBytes = kCtaWarps * kWarpSmemBytes;
 constexpr float kZeroLimit = 2688.0f * 0x1p-100f;   // all-zero block guard on A_b
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -380,68 +378,87 @@ __device__ __forceinline__ void store_block(const Payload& P, int64_t gb, int l4
   }
 }
 
-// Load the lane's part of a payload block: codes of its 4 rows and each row's decode scale.
+// ------------------------------------------------------------------ prefetchable payload reads
+
+// Raw payload words of the lane's part of one block, loaded one tile ahead of their use.
+struct PayRaw {
+  uint32_t code[4][2];
+  uint32_t g[4];   // group-scale bytes: layout B = the block's 16 (G=16) or 8 (G=32) bytes;
+                   // layout A = the lane's own 4 (G=16) or 2 (G=32) bytes in g[0]
+  float sb;
+};
+
+__device__ __forceinline__ void pay_zero(PayRaw& r) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    r.code[k][0] = r.code[k][1] = 0u;
+    r.g[k] = 0u;
+  }
+  r.sb = 0.0f;
+}
+
 template <int G, bool LB>
-__device__ __forceinline__ void load_block(const Payload& P, int64_t gb, int l4, uint32_t code[4][2],
-                                           float S[4]) {
+__device__ __forceinline__ void pay_load(const Payload& P, int64_t gb, int l4, PayRaw& r) {
   if (LB) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       uint2 c = __ldg(reinterpret_cast<const uint2*>(P.codes + gb * 128 + (l4 + 4 * k) * 8));
-      code[k][0] = c.x;
-      code[k][1] = c.y;
+      r.code[k][0] = c.x;
+      r.code[k][1] = c.y;
     }
   } else {
     const uint4* src = reinterpret_cast<const uint4*>(P.codes + gb * 128 + l4 * 32);
     uint4 c0 = __ldg(src), c1 = __ldg(src + 1);
-    code[0][0] = c0.x; code[0][1] = c0.y; code[1][0] = c0.z; code[1][1] = c0.w;
-    code[2][0] = c1.x; code[2][1] = c1.y; code[3][0] = c1.z; code[3][1] = c1.w;
+    r.code[0][0] = c0.x; r.code[0][1] = c0.y; r.code[1][0] = c0.z; r.code[1][1] = c0.w;
+    r.code[2][0] = c1.x; r.code[2][1] = c1.y; r.code[3][0] = c1.z; r.code[3][1] = c1.w;
   }
-  uint32_t sg;   // the 4 rows' group-scale codes, row k in byte k
   if (G == 16) {
     if (LB) {
-      // row l4 + 4k uses byte l4 of word k
       uint4 all = __ldg(reinterpret_cast<const uint4*>(P.gsc + gb * 16));
-      const uint32_t sel = 0x4440u | (uint32_t)l4;
-      sg = __byte_perm(all.x, 0, sel) | (__byte_perm(all.y, 0, sel) << 8) |
-           (__byte_perm(all.z, 0, sel) << 16) | (__byte_perm(all.w, 0, sel) << 24);
+      r.g[0] = all.x; r.g[1] = all.y; r.g[2] = all.z; r.g[3] = all.w;
     } else {
-      sg = __ldg(reinterpret_cast<const uint32_t*>(P.gsc + gb * 16 + 4 * l4));
+      r.g[0] = __ldg(reinterpret_cast<const uint32_t*>(P.gsc + gb * 16 + 4 * l4));
     }
   } else {
     if (LB) {
       uint2 all = __ldg(reinterpret_cast<const uint2*>(P.gsc + gb * 8));
-      // row l4 + 4k belongs to group (l4 >> 1) + 2k: byte (l4 >> 1) + 2(k & 1) of word k >> 1
-      const uint32_t s0 = 0x4440u | (uint32_t)(l4 >> 1), s2 = s0 + 2;
-      sg = __byte_perm(all.x, 0, s0) | (__byte_perm(all.x, 0, s2) << 8) |
-           (__byte_perm(all.y, 0, s0) << 16) | (__byte_perm(all.y, 0, s2) << 24);
+      r.g[0] = all.x; r.g[1] = all.y;
     } else {
-      const uint32_t two = __ldg(reinterpret_cast<const uint16_t*>(P.gsc + gb * 8 + 2 * l4));
-      sg = (two & 0xffu) * 0x0101u | ((two >> 8) & 0xffu) * 0x01010000u;
+      r.g[0] = __ldg(reinterpret_cast<const uint16_t*>(P.gsc + gb * 8 + 2 * l4));
     }
   }
-  const float sb = __ldg(P.bsc + gb);
-  const float2 s01 = e4m3x2_to_f2(sg & 0xffffu), s23 = e4m3x2_to_f2(sg >> 16);
-  S[0] = __fmul_rn(s01.x, sb);
-  S[1] = __fmul_rn(s01.y, sb);
-  S[2] = __fmul_rn(s23.x, sb);
-  S[3] = __fmul_rn(s23.y, sb);
+  r.sb = __ldg(P.bsc + gb);
 }
 
-// Load the lane's 4 rows of bfloat16 input in layout A (64 contiguous elements).
-__device__ __forceinline__ void load_rows_bf16_A(const uint16_t* x, int64_t gb, int a, Rows v) {
-  const uint4* src = reinterpret_cast<const uint4*>(x + gb * kBlock + a * 64);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint4 t = __ldg(src + 2 * k + h);
-      v[k][4 * h + 0] = bf16x2_to_f2(t.x);
-      v[k][4 * h + 1] = bf16x2_to_f2(t.y);
-      v[k][4 * h + 2] = bf16x2_to_f2(t.z);
-      v[k][4 * h + 3] = bf16x2_to_f2(t.w);
+// Decode scale S = value(s_g) * s_b of each of the lane's 4 rows.
+template <int G, bool LB>
+__device__ __forceinline__ void pay_scales(const PayRaw& r, int l4, float S[4]) {
+  uint32_t sg;   // row k's group-scale code in byte k
+  if (G == 16) {
+    if (LB) {
+      // row l4 + 4k uses byte l4 of word k
+      const uint32_t sel = 0x4440u | (uint32_t)l4;
+      sg = __byte_perm(r.g[0], 0, sel) | (__byte_perm(r.g[1], 0, sel) << 8) |
+           (__byte_perm(r.g[2], 0, sel) << 16) | (__byte_perm(r.g[3], 0, sel) << 24);
+    } else {
+      sg = r.g[0];
+    }
+  } else {
+    if (LB) {
+      // row l4 + 4k belongs to group (l4 >> 1) + 2k: byte (l4 >> 1) + 2(k & 1) of word k >> 1
+      const uint32_t s0 = 0x4440u | (uint32_t)(l4 >> 1), s2 = s0 + 2;
+      sg = __byte_perm(r.g[0], 0, s0) | (__byte_perm(r.g[0], 0, s2) << 8) |
+           (__byte_perm(r.g[1], 0, s0) << 16) | (__byte_perm(r.g[1], 0, s2) << 24);
+    } else {
+      // rows 4 l4 + {0,1} form group 2 l4, rows 4 l4 + {2,3} group 2 l4 + 1
+      sg = (r.g[0] & 0xffu) * 0x0101u | ((r.g[0] >> 8) & 0xffu) * 0x01010000u;
     }
   }
+  const float2 s01 = e4m3x2_to_f2(sg & 0xffffu), s23 = e4m3x2_to_f2(sg >> 16);
+  S[0] = __fmul_rn(s01.x, r.sb);
+  S[1] = __fmul_rn(s01.y, r.sb);
+  S[2] = __fmul_rn(s23.x, r.sb);
+  S[3] = __fmul_rn(s23.y, r.sb);
 }
 
 __device__ __forceinline__ void zero_rows(Rows v) {
@@ -451,40 +468,230 @@ __device__ __forceinline__ void zero_rows(Rows v) {
     for (int j = 0; j < 8; ++j) v[k][j] = make_float2(0.0f, 0.0f);
 }
 
-// Accumulate decoded rows (layout A: 64 contiguous elements per lane) into dst.
-template <int DT, int BETA>
-__device__ __forceinline__ void accumulate_A(void* dst, int64_t gb, int a, const Rows v) {
-  if (DT == FP4Q_BF16) {
-    uint4* d = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dst) + gb * kBlock + a * 64);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float2 x0 = v[k][4 * h], x1 = v[k][4 * h + 1], x2 = v[k][4 * h + 2], x3 = v[k][4 * h + 3];
-        if (BETA) {
-          uint4 o = d[2 * k + h];
-          x0 = add2(bf16x2_to_f2(o.x), x0);
-          x1 = add2(bf16x2_to_f2(o.y), x1);
-          x2 = add2(bf16x2_to_f2(o.z), x2);
-          x3 = add2(bf16x2_to_f2(o.w), x3);
-        }
-        d[2 * k + h] = make_uint4(f2_to_bf16x2(x0), f2_to_bf16x2(x1), f2_to_bf16x2(x2), f2_to_bf16x2(x3));
+// ------------------------------------------------------------------ TMA pipelines
+
+// Shared-memory primitives (sm_90+ PTX: mbarrier, cp.async.bulk.tensor, proxy fences).
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// One bounded poll of a barrier phase; the thread may be suspended up to hint_ns.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Device fault word: set when a bounded wait gives up (the kernel then drains its own copies
+// in flight, with a bound, and returns). Read by fp4q_fault_flags.
+__device__ unsigned int g_fp4q_fault;
+constexpr unsigned kFaultLoadWait = 1u;    // a TMA load did not complete within the bound
+constexpr unsigned kFaultDrainWait = 2u;   // a copy still in flight after a fault did not complete
+constexpr unsigned kFaultSelftest = 4u;    // the self-test wait ran out (expected)
+
+// A wait is declared failed after kSpinLimit polls of at most kSuspendHintNs each (~1 s).
+constexpr uint32_t kSpinLimit = 1u << 20;
+constexpr uint32_t kSuspendHintNs = 1000;
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t polls) {
+  for (uint32_t i = 0; i < polls; ++i)
+    if (mbar_try_wait(bar, parity, kSuspendHintNs)) return true;
+  return false;
+}
+
+constexpr int kStages = 3;                 // input tiles in flight per warp
+constexpr int kTileLinesBF16 = 32;         // 128-byte lines per 8-block bf16 tile (4 KiB)
+constexpr int kTileLinesF32 = 64;          // 128-byte lines per 8-block f32 tile (8 KiB)
+constexpr int kXBufBytes = 10240;          // transpose buffer and output staging (>= 9344)
+
+// Per-warp shared memory: [input stages][xbuf][barriers], every part 1024-byte aligned
+// (the 128-byte TMA swizzle repeats every 1024 bytes).
+template <int IN_BYTES>
+struct WarpSmemLayout {
+  static constexpr int kRegion = kStages * IN_BYTES + kXBufBytes + 1024;
+  static constexpr int kCtaBytes = kCtaWarps * kRegion + 1024;
+};
+
+struct WarpSmem {
+  uint32_t stage0, xbuf, bar0;
+  uint8_t* xbuf_ptr;
+};
+
+template <int IN_BYTES>
+__device__ __forceinline__ WarpSmem warp_smem(uint8_t* raw, int warp) {
+  typedef WarpSmemLayout<IN_BYTES> L;
+  const uint32_t raw_s = smem_addr(raw);
+  const uint32_t base = ((raw_s + 1023u) & ~1023u) + (uint32_t)(warp * L::kRegion);
+  WarpSmem w;
+  w.stage0 = base;
+  w.xbuf = base + kStages * IN_BYTES;
+  w.bar0 = w.xbuf + kXBufBytes;
+  w.xbuf_ptr = raw + (w.xbuf - raw_s);
+  return w;
+}
+
+// Per-warp input pipeline: lane 0 keeps kStages tile loads in flight; every lane waits on
+// the tile's barrier, reads it, and the stage is refilled with the tile kStages ahead.
+template <int BYTES, int LINES>
+struct InPipe {
+  uint32_t stage0, bar0;
+  int64_t t0, W, tiles;
+  int i, issued;
+
+  __device__ __forceinline__ uint32_t buf(int s) const { return stage0 + (uint32_t)(s * BYTES); }
+  __device__ __forceinline__ uint32_t bar(int s) const { return bar0 + 8u * (uint32_t)s; }
+
+  __device__ __forceinline__ void issue(const CUtensorMap* map, int s, int64_t t) {
+    mbar_expect_tx(bar(s), BYTES);
+    tma_load_2d(buf(s), map, 0, (int32_t)(t * LINES), bar(s));
+  }
+  __device__ __forceinline__ void start(const WarpSmem& ws, int64_t t0_, int64_t W_, int64_t tiles_,
+                                        const CUtensorMap* map, int lane) {
+    stage0 = ws.stage0;
+    bar0 = ws.bar0;
+    t0 = t0_;
+    W = W_;
+    tiles = tiles_;
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) mbar_init(bar(s), 1);
+      fence_barrier_init();
+    }
+    __syncwarp();
+    issued = 0;
+    for (int s = 0; s < kStages; ++s) {
+      const int64_t t = t0 + (int64_t)s * W;
+      if (t < tiles) {
+        if (lane == 0) issue(map, s, t);
+        ++issued;
       }
     }
-  } else {
-    float4* d = reinterpret_cast<float4*>(static_cast<float*>(dst) + gb * kBlock + a * 64);
+    i = 0;
+  }
+  __device__ __forceinline__ uint32_t cur() const { return buf(i % kStages); }
+  // Wait for the current tile. On failure record the fault, wait (bounded) for every copy
+  // still in flight into this warp's stages, and return false: the caller must return.
+  __device__ __forceinline__ bool wait() {
+    bool ok = mbar_wait(bar(i % kStages), (uint32_t)((i / kStages) & 1), kSpinLimit);
+    ok = __all_sync(kFull, ok);
+    if (!ok) {
+      if ((threadIdx.x & 31) == 0) atomicOr(&g_fp4q_fault, kFaultLoadWait);
+      for (int k = i; k < issued; ++k)
+        if (!mbar_wait(bar(k % kStages), (uint32_t)((k / kStages) & 1), kSpinLimit) && (threadIdx.x & 31) == 0)
+          atomicOr(&g_fp4q_fault, kFaultDrainWait);
+    }
+    return ok;
+  }
+  // The current stage has been read: refill it with the tile kStages iterations ahead. The
+  // lanes' shared-memory reads (generic proxy) must be ordered before the TMA write (async
+  // proxy) into the same stage: every lane fences across proxies, then the warp syncs, then
+  // lane 0 issues the copy. Without the fence a refill overtook an outstanding read.
+  __device__ __forceinline__ void refill(const CUtensorMap* map, int lane) {
+    fence_proxy_async();
+    __syncwarp();
+    const int64_t tn = t0 + (int64_t)(i + kStages) * W;
+    if (tn < tiles) {
+      if (lane == 0) issue(map, i % kStages, tn);
+      ++issued;
+    }
+    ++i;
+  }
+};
+
+// Tile I/O in the 128-byte-swizzled shared layout the TMA writes and reads: 16-byte chunk c
+// of line l sits at chunk position c ^ (l & 7). Layout A: lane (blk, a) owns line 4 blk + a
+// of a bf16 tile (its 4 rows), or lines 8 blk + 2a + {0, 1} of an f32 tile.
+__device__ __forceinline__ void tile_read_bf16(uint32_t buf, int blk, int a, Rows v) {
+  const int line = 4 * blk + a;
+  const uint32_t base = buf + (uint32_t)line * 128u, sw = (uint32_t)(line & 7);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+  for (int c = 0; c < 8; ++c) {
+    const uint4 t = lds128(base + ((((uint32_t)c) ^ sw) << 4));
+    const int k = c >> 1, j = 4 * (c & 1);
+    v[k][j + 0] = bf16x2_to_f2(t.x);
+    v[k][j + 1] = bf16x2_to_f2(t.y);
+    v[k][j + 2] = bf16x2_to_f2(t.z);
+    v[k][j + 3] = bf16x2_to_f2(t.w);
+  }
+}
+__device__ __forceinline__ void tile_write_bf16(uint32_t buf, int blk, int a, const Rows v) {
+  const int line = 4 * blk + a;
+  const uint32_t base = buf + (uint32_t)line * 128u, sw = (uint32_t)(line & 7);
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float2 x0 = v[k][2 * h], x1 = v[k][2 * h + 1];
-        if (BETA) {
-          float4 o = d[4 * k + h];
-          x0 = add2(make_float2(o.x, o.y), x0);
-          x1 = add2(make_float2(o.z, o.w), x1);
-        }
-        d[4 * k + h] = make_float4(x0.x, x0.y, x1.x, x1.y);
-      }
+  for (int c = 0; c < 8; ++c) {
+    const int k = c >> 1, j = 4 * (c & 1);
+    sts128(base + ((((uint32_t)c) ^ sw) << 4),
+           make_uint4(f2_to_bf16x2(v[k][j]), f2_to_bf16x2(v[k][j + 1]), f2_to_bf16x2(v[k][j + 2]),
+                      f2_to_bf16x2(v[k][j + 3])));
+  }
+}
+__device__ __forceinline__ void tile_read_f32(uint32_t buf, int blk, int a, Rows v) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int line = 8 * blk + 2 * a + (k >> 1);
+    const uint32_t base = buf + (uint32_t)line * 128u, sw = (uint32_t)(line & 7);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const uint32_t c = (uint32_t)(4 * (k & 1) + cc);
+      const uint4 t = lds128(base + ((c ^ sw) << 4));
+      v[k][2 * cc] = make_float2(__uint_as_float(t.x), __uint_as_float(t.y));
+      v[k][2 * cc + 1] = make_float2(__uint_as_float(t.z), __uint_as_float(t.w));
+    }
+  }
+}
+__device__ __forceinline__ void tile_write_f32(uint32_t buf, int blk, int a, const Rows v) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int line = 8 * blk + 2 * a + (k >> 1);
+    const uint32_t base = buf + (uint32_t)line * 128u, sw = (uint32_t)(line & 7);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const uint32_t c = (uint32_t)(4 * (k & 1) + cc);
+      sts128(base + ((c ^ sw) << 4),
+             make_uint4(__float_as_uint(v[k][2 * cc].x), __float_as_uint(v[k][2 * cc].y),
+                        __float_as_uint(v[k][2 * cc + 1].x), __float_as_uint(v[k][2 * cc + 1].y)));
     }
   }
 }
@@ -501,24 +708,45 @@ __device__ __forceinline__ int64_t warp_global() {
 }
 __device__ __forceinline__ int64_t warp_count() { return (int64_t)gridDim.x * kCtaWarps; }
 
-// K1: compress. x (bfloat16, n) -> payload.
+// Lane 0 of the warp waits until its last TMA store has finished reading the staging buffer.
+__device__ __forceinline__ void staging_free(int lane) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+}
+// Publish the staging buffer (written with st.shared) to the TMA store of tile t.
+__device__ __forceinline__ void staging_store(const CUtensorMap* map, int lines, int64_t t, uint32_t xbuf,
+                                              int lane) {
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, 0, (int32_t)(t * lines), xbuf);
+    bulk_commit();
+  }
+}
+
+// K1: compress. x (bfloat16, n) -> payload. Input tiles arrive by TMA.
 template <int G, int FWHT>
 __global__ void __launch_bounds__(kCtaWarps * 32)
-compress_kernel(const uint16_t* __restrict__ x, Payload P, TileLoop T) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  float4* buf = reinterpret_cast<float4*>(smem + (threadIdx.x >> 5) * kWarpSmemBytes);
-  const int lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  for (int64_t t = warp_global(); t < T.tiles; t += warp_count()) {
+compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T) {
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
+  const WarpSmem ws = warp_smem<4096>(smem_raw, warp);
+  float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
+  InPipe<4096, kTileLinesBF16> pipe;
+  pipe.start(ws, warp_global(), warp_count(), T.tiles, &xmap, lane);
+  for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     const int64_t gb = t * kTileBlocks + blk;
     const bool valid = gb < T.nb;
+    if (!pipe.wait()) return;
     Rows v;
-    if (valid) load_rows_bf16_A(x, gb, l4, v); else zero_rows(v);
+    tile_read_bf16(pipe.cur(), blk, l4, v);
+    pipe.refill(&xmap, lane);
     Quant q;
     if (FWHT) {
       level1_fwd(v);
       rows_bfly(v, 1);             // h = 16
       rows_bfly(v, 2);             // h = 32
-      transpose<true>(v, buf, blk, l4);
+      transpose<true>(v, tbuf, blk, l4);
       rows_bfly(v, 1);             // h = 64
       rows_bfly(v, 2);             // h = 128
       quantize<G, true, true>(v, q);
@@ -531,66 +759,93 @@ compress_kernel(const uint16_t* __restrict__ x, Payload P, TileLoop T) {
 }
 
 // K2: decompress-accumulate. payload -> dst (dtype DT), dst = BETA ? dst + x^ : x^.
+// The payload of the next tile is prefetched into registers; dst tiles are read (BETA) and
+// written through the swizzled shared staging buffer by TMA.
 template <int G, int FWHT, int DT, int BETA>
 __global__ void __launch_bounds__(kCtaWarps * 32)
-decompress_kernel(Payload P, void* __restrict__ dst, TileLoop T) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  float4* buf = reinterpret_cast<float4*>(smem + (threadIdx.x >> 5) * kWarpSmemBytes);
-  const int lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  for (int64_t t = warp_global(); t < T.tiles; t += warp_count()) {
-    const int64_t gb = t * kTileBlocks + blk;
-    const bool valid = gb < T.nb;
-    uint32_t code[4][2];
+decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop T) {
+  constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
+  constexpr int LINES = DT == FP4Q_BF16 ? kTileLinesBF16 : kTileLinesF32;
+  constexpr bool LB = FWHT != 0;
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
+  const WarpSmem ws = warp_smem<BETA ? TB : 0>(smem_raw, warp);
+  float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
+  InPipe<TB, LINES> pipe;
+  const int64_t t0 = warp_global(), W = warp_count();
+  if (BETA) pipe.start(ws, t0, W, T.tiles, &dmap, lane);
+  PayRaw cur, nxt;
+  if (t0 < T.tiles && t0 * kTileBlocks + blk < T.nb) pay_load<G, LB>(P, t0 * kTileBlocks + blk, l4, cur);
+  else pay_zero(cur);
+  for (int64_t t = t0; t < T.tiles; t += W) {
+    const int64_t tn = t + W, gbn = tn * kTileBlocks + blk;
+    if (tn < T.tiles && gbn < T.nb) pay_load<G, LB>(P, gbn, l4, nxt); else pay_zero(nxt);
     float S[4];
+    pay_scales<G, LB>(cur, l4, S);
     Rows v;
+    dequantize(cur.code, S, v);
+    staging_free(lane);
     if (FWHT) {
-      if (valid) {
-        load_block<G, true>(P, gb, l4, code, S);
-        dequantize(code, S, v);
-      } else {
-        zero_rows(v);
-      }
       rows_bfly(v, 2);             // h = 128
       rows_bfly(v, 1);             // h = 64
-      transpose<false>(v, buf, blk, l4);
+      transpose<false>(v, tbuf, blk, l4);
       rows_bfly(v, 2);             // h = 32
       rows_bfly(v, 1);             // h = 16
       level1_inv(v);
       scale16<BETA != 0>(v);
-    } else {
-      if (!valid) continue;
-      load_block<G, false>(P, gb, l4, code, S);
-      dequantize(code, S, v);
     }
-    if (valid) accumulate_A<DT, BETA>(dst, gb, l4, v);
+    if (BETA) {
+      if (!pipe.wait()) break;
+      Rows d;
+      if (DT == FP4Q_BF16) tile_read_bf16(pipe.cur(), blk, l4, d); else tile_read_f32(pipe.cur(), blk, l4, d);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[k][j] = add2(d[k][j], v[k][j]);
+      pipe.refill(&dmap, lane);
+    }
+    if (DT == FP4Q_BF16) tile_write_bf16(ws.xbuf, blk, l4, v); else tile_write_f32(ws.xbuf, blk, l4, v);
+    staging_store(&dmap, LINES, t, ws.xbuf, lane);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      cur.code[k][0] = nxt.code[k][0];
+      cur.code[k][1] = nxt.code[k][1];
+      cur.g[k] = nxt.g[k];
+    }
+    cur.sb = nxt.sb;
   }
+  if (lane == 0) bulk_wait_all();
 }
 
 // K3: fused roundtrip. x (bfloat16) -> y = bf16(decode(compress(x))), no payload.
 template <int G, int FWHT>
 __global__ void __launch_bounds__(kCtaWarps * 32)
-roundtrip_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y, TileLoop T) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  float4* buf = reinterpret_cast<float4*>(smem + (threadIdx.x >> 5) * kWarpSmemBytes);
-  const int lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  for (int64_t t = warp_global(); t < T.tiles; t += warp_count()) {
-    const int64_t gb = t * kTileBlocks + blk;
-    const bool valid = gb < T.nb;
+roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap, TileLoop T) {
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
+  const WarpSmem ws = warp_smem<4096>(smem_raw, warp);
+  float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
+  InPipe<4096, kTileLinesBF16> pipe;
+  pipe.start(ws, warp_global(), warp_count(), T.tiles, &xmap, lane);
+  for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
+    if (!pipe.wait()) break;
     Rows v;
-    if (valid) load_rows_bf16_A(x, gb, l4, v); else zero_rows(v);
+    tile_read_bf16(pipe.cur(), blk, l4, v);
+    pipe.refill(&xmap, lane);
     Quant q;
     if (FWHT) {
       level1_fwd(v);
       rows_bfly(v, 1);
       rows_bfly(v, 2);
-      transpose<true>(v, buf, blk, l4);
+      staging_free(lane);
+      transpose<true>(v, tbuf, blk, l4);
       rows_bfly(v, 1);
       rows_bfly(v, 2);
       quantize<G, true, true>(v, q);
       dequantize(q.code, q.S, v);
       rows_bfly(v, 2);
       rows_bfly(v, 1);
-      transpose<false>(v, buf, blk, l4);
+      transpose<false>(v, tbuf, blk, l4);
       rows_bfly(v, 2);
       rows_bfly(v, 1);
       level1_inv(v);
@@ -598,9 +853,12 @@ roundtrip_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y, TileL
     } else {
       quantize<G, false, false>(v, q);
       dequantize(q.code, q.S, v);
+      staging_free(lane);
     }
-    if (valid) accumulate_A<FP4Q_BF16, 0>(y, gb, l4, v);
+    tile_write_bf16(ws.xbuf, blk, l4, v);
+    staging_store(&ymap, kTileLinesBF16, t, ws.xbuf, lane);
   }
+  if (lane == 0) bulk_wait_all();
 }
 
 // K4: emulated R-way reduce. R payloads -> transform-domain FP32 sum in rank order ->
@@ -618,16 +876,18 @@ reduce_kernel(RankPtrs in, int R, int64_t n, Payload out, TileLoop T) {
     const bool valid = gb < T.nb;
     Rows z;
     if (valid) {
-      uint32_t code[4][2];
+      PayRaw raw;
       float S[4];
-      load_block<G, false>(payload_of(const_cast<uint8_t*>(in.p[0]), n, G), gb, l4, code, S);
-      dequantize(code, S, z);
+      pay_load<G, false>(payload_of(const_cast<uint8_t*>(in.p[0]), n, G), gb, l4, raw);
+      pay_scales<G, false>(raw, l4, S);
+      dequantize(raw.code, S, z);
 #pragma unroll
       for (int r = 1; r < FP4Q_MAX_RANKS; ++r) {
         if (r >= R) break;
         Rows xr;
-        load_block<G, false>(payload_of(const_cast<uint8_t*>(in.p[r]), n, G), gb, l4, code, S);
-        dequantize(code, S, xr);
+        pay_load<G, false>(payload_of(const_cast<uint8_t*>(in.p[r]), n, G), gb, l4, raw);
+        pay_scales<G, false>(raw, l4, S);
+        dequantize(raw.code, S, xr);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
@@ -642,12 +902,21 @@ reduce_kernel(RankPtrs in, int R, int64_t n, Payload out, TileLoop T) {
   }
 }
 
-// ------------------------------------------------------------------ host side
+// Self-test of the bounded wait: one warp waits on a barrier phase that nothing completes;
+// the wait gives up after `polls` polls and records kFaultSelftest.
+__global__ void selftest_wait_kernel(uint32_t polls) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(b, 0u, polls);
+  if (!__all_sync(kFull, ok) && threadIdx.x == 0) atomicOr(&g_fp4q_fault, kFaultSelftest);
+}
 
-struct Launch {
-  int grid;
-  int smem;
-};
+// ------------------------------------------------------------------ host side
 
 int g_num_sms[64];
 
@@ -661,6 +930,11 @@ int num_sms() {
   }
   return g_num_sms[dev];
 }
+
+struct Launch {
+  int grid;
+  int smem;
+};
 
 // Persistent grid: as many CTAs as fit on all SMs at once, never more than the tiles need.
 template <typename K>
@@ -681,8 +955,39 @@ fp4q_status plan(K kernel, int smem, int64_t tiles, Launch& L) {
   return FP4Q_OK;
 }
 
-fp4q_status launched() {
-  return cudaGetLastError() == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+fp4q_status launched() { return cudaGetLastError() == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA; }
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+typedef CUresult (*EncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = []() -> EncodeTiled {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
+}
+
+// 2-D view of a contiguous buffer as 128-byte lines, one 8-block tile per box, 128-byte
+// swizzle (bfloat16: 64 elements per line, 32 lines per tile; float32: 32 and 64).
+bool line_map(CUtensorMap* m, const void* ptr, int64_t n, bool f32) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t per_line = f32 ? 32 : 64;
+  const cuuint64_t dims[2] = {per_line, (cuuint64_t)(n / (int64_t)per_line)};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {(cuuint32_t)per_line, (cuuint32_t)(f32 ? kTileLinesF32 : kTileLinesBF16)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 fp4q_status check_params(const fp4q_params* p, int& G, int& fwht) {
@@ -695,7 +1000,8 @@ fp4q_status check_params(const fp4q_params* p, int& G, int& fwht) {
   return FP4Q_OK;
 }
 
-bool size_ok(int64_t n) { return n > 0 && n % FP4Q_BLOCK == 0 && n < ((int64_t)1 << 40); }
+// The kernels address tiles with 32-bit TMA line coordinates: n < 2^37 keeps them in range.
+bool size_ok(int64_t n) { return n > 0 && n % FP4Q_BLOCK == 0 && n < ((int64_t)1 << 37); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -712,33 +1018,40 @@ TileLoop tiles_of(int64_t n) {
 template <int G, int F>
 fp4q_status launch_compress(const void* x, int64_t n, void* payload, cudaStream_t s) {
   TileLoop T = tiles_of(n);
+  CUtensorMap xm;
+  if (!line_map(&xm, x, n, false)) return FP4Q_ERR_CUDA;
   auto k = compress_kernel<G, F>;
   Launch L;
-  fp4q_status st = plan(k, F ? kCtaSmemBytes : 0, T.tiles, L);
+  fp4q_status st = plan(k, WarpSmemLayout<4096>::kCtaBytes, T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(static_cast<const uint16_t*>(x), payload_of(payload, n, G), T);
+  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(xm, payload_of(payload, n, G), T);
   return launched();
 }
 
 template <int G, int F, int DT, int B>
 fp4q_status launch_decompress(const void* payload, int64_t n, void* dst, cudaStream_t s) {
   TileLoop T = tiles_of(n);
+  CUtensorMap dm;
+  if (!line_map(&dm, dst, n, DT == FP4Q_F32)) return FP4Q_ERR_CUDA;
   auto k = decompress_kernel<G, F, DT, B>;
+  constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
   Launch L;
-  fp4q_status st = plan(k, F ? kCtaSmemBytes : 0, T.tiles, L);
+  fp4q_status st = plan(k, WarpSmemLayout<B ? TB : 0>::kCtaBytes, T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(payload_of(const_cast<void*>(payload), n, G), dst, T);
+  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(dm, payload_of(const_cast<void*>(payload), n, G), T);
   return launched();
 }
 
 template <int G, int F>
 fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) {
   TileLoop T = tiles_of(n);
+  CUtensorMap xm, ym;
+  if (!line_map(&xm, x, n, false) || !line_map(&ym, y, n, false)) return FP4Q_ERR_CUDA;
   auto k = roundtrip_kernel<G, F>;
   Launch L;
-  fp4q_status st = plan(k, F ? kCtaSmemBytes : 0, T.tiles, L);
+  fp4q_status st = plan(k, WarpSmemLayout<4096>::kCtaBytes, T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), T);
+  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(xm, ym, T);
   return launched();
 }
 
@@ -862,19 +1175,37 @@ fp4q_status fp4q_reduce_requantize(const void* const* payloads, int32_t R, int64
   return G == 16 ? launch_reduce<16>(in, R, n, out_payload, s) : launch_reduce<32>(in, R, n, out_payload, s);
 }
 
+fp4q_status fp4q_fault_flags(uint32_t* flags, int32_t clear) {
+  if (!flags) return FP4Q_ERR_NULL;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fp4q_fault, sizeof(v)) != cudaSuccess) return FP4Q_ERR_CUDA;
+  *flags = v;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_fp4q_fault, &zero, sizeof(zero)) != cudaSuccess) return FP4Q_ERR_CUDA;
+  }
+  return FP4Q_OK;
+}
+
+fp4q_status fp4q_selftest_wait_timeout(uint32_t polls, void* stream) {
+  if (polls == 0 || polls > (1u << 20)) return FP4Q_ERR_PARAM;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(polls);
+  return launched();
+}
+
 const char* fp4q_status_string(fp4q_status status) {
   switch (status) {
     case FP4Q_OK: return "ok";
     case FP4Q_ERR_NULL: return "null pointer";
-    case FP4Q_ERR_SIZE: return "n must be a positive multiple of 256 below 2^40";
+    case FP4Q_ERR_SIZE: return "n must be a positive multiple of 256 below 2^37";
     case FP4Q_ERR_ALIGN: return "pointer not 16-byte aligned";
-    case FP4Q_ERR_PARAM: return "invalid parameter (group, block, fwht, R, dtype or beta)";
+    case FP4Q_ERR_PARAM: return "invalid parameter (group, block, fwht, R, dtype, beta or polls)";
     case FP4Q_ERR_OVERLAP: return "output overlaps an input";
     case FP4Q_ERR_CUDA: return "CUDA runtime error or failed launch";
   }
   return "unknown status";
 }
 
-int32_t fp4q_version(void) { return 100; }
+int32_t fp4q_version(void) { return 200; }
 
 }  // extern "C"

@@ -62,7 +62,8 @@
  * Preconditions on data (not checked): inputs finite and |x| < 2^120.
  *
  * Threading and ownership: the caller owns every buffer; the library keeps no per-call
- * state and allocates no device memory. All entry points are asynchronous on the given
+ * state and allocates no device memory (its only device data is the 4-byte fault word read
+ * by fp4q_fault_flags). All entry points are asynchronous on the given
  * stream and never synchronise. Argument errors are returned before anything is launched.
  * A failed launch returns FP4Q_ERR_CUDA (the CUDA error is left to the caller's next
  * runtime call to report).
@@ -87,7 +88,7 @@ extern "C" {
 typedef enum fp4q_status {
   FP4Q_OK = 0,
   FP4Q_ERR_NULL = 1,     /* a required pointer is NULL                                  */
-  FP4Q_ERR_SIZE = 2,     /* n <= 0, n % 256 != 0, or n >= 2^40                          */
+  FP4Q_ERR_SIZE = 2,     /* n <= 0, n % 256 != 0, or n >= 2^37                          */
   FP4Q_ERR_ALIGN = 3,    /* a data pointer is not 16-byte aligned                       */
   FP4Q_ERR_PARAM = 4,    /* bad params: group not 16/32, block not 256, fwht not 0/1,
                             R outside [1, 8], unknown dtype, beta not 0/1               */
@@ -146,6 +147,22 @@ fp4q_status fp4q_roundtrip(const void* x_bf16, int64_t n, void* y_bf16,
 fp4q_status fp4q_reduce_requantize(const void* const* payloads, int32_t R, int64_t n,
                                    void* out_payload, const fp4q_params* params,
                                    void* stream);
+
+/* Device fault word of the current device. The kernels wait on TMA copies with bounded
+ * waits (about a second); a wait that gives up sets a bit here, waits (bounded) for the
+ * warp's copies still in flight and returns early, leaving that call's outputs incomplete:
+ *   bit 0: a TMA load did not complete within the bound;
+ *   bit 1: a copy still in flight after such a fault did not complete either;
+ *   bit 2: fp4q_selftest_wait_timeout ran out (expected).
+ * The word is sticky across calls. This call synchronises with the device (it reads device
+ * memory); clear != 0 resets the word to 0 afterwards. No counterpart in the pages: it
+ * reports the health of this implementation's asynchronous copies. */
+fp4q_status fp4q_fault_flags(uint32_t* flags, int32_t clear);
+
+/* Self-test of the bounded wait: launches one warp that waits on a barrier phase nothing
+ * completes, giving up after `polls` polls (1 <= polls <= 2^20) and setting bit 2 of the
+ * fault word. Asynchronous on `stream`. No counterpart in the pages. */
+fp4q_status fp4q_selftest_wait_timeout(uint32_t polls, void* stream);
 
 /* Static string naming a status code (never NULL). */
 const char* fp4q_status_string(fp4q_status status);

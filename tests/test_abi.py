@@ -55,7 +55,7 @@ def test_payload_layout_matches_oracle(L, n, G):
 
 def test_payload_bytes_defaults_and_invalid(L):
     assert L.fp4q_payload_bytes(4096, None) == 2368
-    for n in (0, -256, 100, 1 << 40):
+    for n in (0, -256, 100, 1 << 37, 1 << 40):
         assert L.fp4q_payload_bytes(n, None) == 0
     for g, b, f in [(8, 256, 1), (16, 128, 1), (16, 256, 2), (64, 256, 0)]:
         assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(g, b, f))) == 0
@@ -71,7 +71,7 @@ def test_compress_argument_errors(L):
     pp = ctypes.byref(P)
     assert L.fp4q_compress(None, 4096, B, pp, None) == _lib.ERR_NULL
     assert L.fp4q_compress(A, 4096, None, pp, None) == _lib.ERR_NULL
-    for n in (0, -256, 100, 4095, 1 << 40):
+    for n in (0, -256, 100, 4095, 1 << 37, 1 << 40):
         assert L.fp4q_compress(A, n, B, pp, None) == _lib.ERR_SIZE
     assert L.fp4q_compress(A + 8, 4096, B, pp, None) == _lib.ERR_ALIGN
     assert L.fp4q_compress(A, 4096, B + 2, pp, None) == _lib.ERR_ALIGN
@@ -134,3 +134,9 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _lib.lib()
+
+
+def test_fault_and_selftest_argument_errors(L):
+    assert L.fp4q_fault_flags(None, 0) == _lib.ERR_NULL
+    assert L.fp4q_selftest_wait_timeout(0, None) == _lib.ERR_PARAM
+    assert L.fp4q_selftest_wait_timeout((1 << 20) + 1, None) == _lib.ERR_PARAM
