@@ -83,6 +83,13 @@ __device__ __forceinline__ void bfly_in(float2& v) {
   v = make_float2(s, d);
 }
 
+// Three-input maximum (sm_100 family), used for the absolute-maximum trees.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // ------------------------------------------------------------------ format conversions
 
 // bfloat16 pair (low half = even element) -> float2, exact.
@@ -230,12 +237,17 @@ __device__ __forceinline__ void quantize(const Rows v, Quant& o) {
   float am[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    float m = 0.0f;
+    float a[16];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(v[k][j].x), fabsf(v[k][j].y)));
-    am[k] = m;
+    for (int j = 0; j < 8; ++j) {
+      a[2 * j] = fabsf(v[k][j].x);
+      a[2 * j + 1] = fabsf(v[k][j].y);
+    }
+    const float m0 = max3(a[0], a[1], a[2]), m1 = max3(a[3], a[4], a[5]), m2 = max3(a[6], a[7], a[8]);
+    const float m3 = max3(a[9], a[10], a[11]), m4 = max3(a[12], a[13], a[14]);
+    am[k] = max3(max3(m0, m1, m2), fmaxf(m3, m4), a[15]);
   }
-  float A = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
+  float A = max3(fmaxf(am[0], am[1]), am[2], am[3]);
   A = fmaxf(A, __shfl_xor_sync(kFull, A, 1));
   A = fmaxf(A, __shfl_xor_sync(kFull, A, 2));
   if (G == 32) {
@@ -461,13 +473,6 @@ __device__ __forceinline__ void pay_scales(const PayRaw& r, int l4, float S[4]) 
   S[3] = __fmul_rn(s23.y, r.sb);
 }
 
-__device__ __forceinline__ void zero_rows(Rows v) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[k][j] = make_float2(0.0f, 0.0f);
-}
-
 // ------------------------------------------------------------------ TMA pipelines
 
 // Shared-memory primitives (sm_90+ PTX: mbarrier, cp.async.bulk.tensor, proxy fences).
@@ -505,6 +510,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* map, int32_t c0, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(src)
@@ -518,6 +529,16 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
   return v;
 }
 __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
@@ -542,16 +563,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   return false;
 }
 
-constexpr int kStages = 3;                 // input tiles in flight per warp
+constexpr int kStages = 2;                 // input tiles in flight per warp
 constexpr int kTileLinesBF16 = 32;         // 128-byte lines per 8-block bf16 tile (4 KiB)
 constexpr int kTileLinesF32 = 64;          // 128-byte lines per 8-block f32 tile (8 KiB)
-constexpr int kXBufBytes = 10240;          // transpose buffer and output staging (>= 9344)
+constexpr int kXBufBytes = 10240;          // transpose buffer / output staging + barriers
+constexpr int kXBufUsed = kUnitsPerBlock * 16 * kTileBlocks;   // 9344 bytes of transpose data
 
-// Per-warp shared memory: [input stages][xbuf][barriers], every part 1024-byte aligned
-// (the 128-byte TMA swizzle repeats every 1024 bytes).
+// Per-warp shared memory: [input stages][xbuf], every part 1024-byte aligned (the 128-byte
+// TMA swizzle repeats every 1024 bytes); the stage barriers sit in the xbuf's unused tail.
 template <int IN_BYTES>
 struct WarpSmemLayout {
-  static constexpr int kRegion = kStages * IN_BYTES + kXBufBytes + 1024;
+  static constexpr int kRegion = kStages * IN_BYTES + kXBufBytes;
   static constexpr int kCtaBytes = kCtaWarps * kRegion + 1024;
 };
 
@@ -568,14 +590,16 @@ __device__ __forceinline__ WarpSmem warp_smem(uint8_t* raw, int warp) {
   WarpSmem w;
   w.stage0 = base;
   w.xbuf = base + kStages * IN_BYTES;
-  w.bar0 = w.xbuf + kXBufBytes;
+  w.bar0 = w.xbuf + kXBufUsed;
   w.xbuf_ptr = raw + (w.xbuf - raw_s);
   return w;
 }
 
-// Per-warp input pipeline: lane 0 keeps kStages tile loads in flight; every lane waits on
-// the tile's barrier, reads it, and the stage is refilled with the tile kStages ahead.
-template <int BYTES, int LINES>
+// Per-warp input pipeline over STAGES stage buffers of BYTES bytes: lane 0 keeps STAGES
+// tiles in flight (issue(buf, bar, t) arms the barrier and starts the copies of tile t);
+// every lane waits on the tile's barrier, reads the stage, and the stage is refilled with
+// the tile STAGES iterations ahead.
+template <int STAGES, int BYTES>
 struct InPipe {
   uint32_t stage0, bar0;
   int64_t t0, W, tiles;
@@ -584,56 +608,54 @@ struct InPipe {
   __device__ __forceinline__ uint32_t buf(int s) const { return stage0 + (uint32_t)(s * BYTES); }
   __device__ __forceinline__ uint32_t bar(int s) const { return bar0 + 8u * (uint32_t)s; }
 
-  __device__ __forceinline__ void issue(const CUtensorMap* map, int s, int64_t t) {
-    mbar_expect_tx(bar(s), BYTES);
-    tma_load_2d(buf(s), map, 0, (int32_t)(t * LINES), bar(s));
-  }
-  __device__ __forceinline__ void start(const WarpSmem& ws, int64_t t0_, int64_t W_, int64_t tiles_,
-                                        const CUtensorMap* map, int lane) {
-    stage0 = ws.stage0;
-    bar0 = ws.bar0;
+  template <class Issue>
+  __device__ __forceinline__ void start(uint32_t stage0_, uint32_t bar0_, int64_t t0_, int64_t W_,
+                                        int64_t tiles_, int lane, Issue&& issue) {
+    stage0 = stage0_;
+    bar0 = bar0_;
     t0 = t0_;
     W = W_;
     tiles = tiles_;
     if (lane == 0) {
-      for (int s = 0; s < kStages; ++s) mbar_init(bar(s), 1);
+      for (int s = 0; s < STAGES; ++s) mbar_init(bar(s), 1);
       fence_barrier_init();
     }
     __syncwarp();
     issued = 0;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       const int64_t t = t0 + (int64_t)s * W;
       if (t < tiles) {
-        if (lane == 0) issue(map, s, t);
+        if (lane == 0) issue(buf(s), bar(s), t);
         ++issued;
       }
     }
     i = 0;
   }
-  __device__ __forceinline__ uint32_t cur() const { return buf(i % kStages); }
+  __device__ __forceinline__ uint32_t cur() const { return buf(i % STAGES); }
   // Wait for the current tile. On failure record the fault, wait (bounded) for every copy
-  // still in flight into this warp's stages, and return false: the caller must return.
+  // still in flight into this warp's stages, and return false: the caller must stop.
   __device__ __forceinline__ bool wait() {
-    bool ok = mbar_wait(bar(i % kStages), (uint32_t)((i / kStages) & 1), kSpinLimit);
+    bool ok = mbar_wait(bar(i % STAGES), (uint32_t)((i / STAGES) & 1), kSpinLimit);
     ok = __all_sync(kFull, ok);
     if (!ok) {
       if ((threadIdx.x & 31) == 0) atomicOr(&g_fp4q_fault, kFaultLoadWait);
       for (int k = i; k < issued; ++k)
-        if (!mbar_wait(bar(k % kStages), (uint32_t)((k / kStages) & 1), kSpinLimit) && (threadIdx.x & 31) == 0)
+        if (!mbar_wait(bar(k % STAGES), (uint32_t)((k / STAGES) & 1), kSpinLimit) && (threadIdx.x & 31) == 0)
           atomicOr(&g_fp4q_fault, kFaultDrainWait);
     }
     return ok;
   }
-  // The current stage has been read: refill it with the tile kStages iterations ahead. The
+  // The current stage has been read: refill it with the tile STAGES iterations ahead. The
   // lanes' shared-memory reads (generic proxy) must be ordered before the TMA write (async
   // proxy) into the same stage: every lane fences across proxies, then the warp syncs, then
   // lane 0 issues the copy. Without the fence a refill overtook an outstanding read.
-  __device__ __forceinline__ void refill(const CUtensorMap* map, int lane) {
+  template <class Issue>
+  __device__ __forceinline__ void refill(int lane, Issue&& issue) {
     fence_proxy_async();
     __syncwarp();
-    const int64_t tn = t0 + (int64_t)(i + kStages) * W;
+    const int64_t tn = t0 + (int64_t)(i + STAGES) * W;
     if (tn < tiles) {
-      if (lane == 0) issue(map, i % kStages, tn);
+      if (lane == 0) issue(buf(i % STAGES), bar(i % STAGES), tn);
       ++issued;
     }
     ++i;
@@ -732,15 +754,19 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<4096>(smem_raw, warp);
   float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
-  InPipe<4096, kTileLinesBF16> pipe;
-  pipe.start(ws, warp_global(), warp_count(), T.tiles, &xmap, lane);
+  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
+    mbar_expect_tx(bar, 4096);
+    tma_load_2d(buf, &xmap, 0, (int32_t)(t * kTileLinesBF16), bar);
+  };
+  InPipe<kStages, 4096> pipe{};
+  pipe.start(ws.stage0, ws.bar0, warp_global(), warp_count(), T.tiles, lane, issue);
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     const int64_t gb = t * kTileBlocks + blk;
     const bool valid = gb < T.nb;
     if (!pipe.wait()) return;
     Rows v;
     tile_read_bf16(pipe.cur(), blk, l4, v);
-    pipe.refill(&xmap, lane);
+    pipe.refill(lane, issue);
     Quant q;
     if (FWHT) {
       level1_fwd(v);
@@ -771,9 +797,13 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<BETA ? TB : 0>(smem_raw, warp);
   float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
-  InPipe<TB, LINES> pipe;
+  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
+    mbar_expect_tx(bar, TB);
+    tma_load_2d(buf, &dmap, 0, (int32_t)(t * LINES), bar);
+  };
+  InPipe<kStages, TB> pipe{};
   const int64_t t0 = warp_global(), W = warp_count();
-  if (BETA) pipe.start(ws, t0, W, T.tiles, &dmap, lane);
+  if (BETA) pipe.start(ws.stage0, ws.bar0, t0, W, T.tiles, lane, issue);
   PayRaw cur, nxt;
   if (t0 < T.tiles && t0 * kTileBlocks + blk < T.nb) pay_load<G, LB>(P, t0 * kTileBlocks + blk, l4, cur);
   else pay_zero(cur);
@@ -802,7 +832,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
       for (int k = 0; k < 4; ++k)
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[k][j] = add2(d[k][j], v[k][j]);
-      pipe.refill(&dmap, lane);
+      pipe.refill(lane, issue);
     }
     if (DT == FP4Q_BF16) tile_write_bf16(ws.xbuf, blk, l4, v); else tile_write_f32(ws.xbuf, blk, l4, v);
     staging_store(&dmap, LINES, t, ws.xbuf, lane);
@@ -825,13 +855,17 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<4096>(smem_raw, warp);
   float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
-  InPipe<4096, kTileLinesBF16> pipe;
-  pipe.start(ws, warp_global(), warp_count(), T.tiles, &xmap, lane);
+  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
+    mbar_expect_tx(bar, 4096);
+    tma_load_2d(buf, &xmap, 0, (int32_t)(t * kTileLinesBF16), bar);
+  };
+  InPipe<kStages, 4096> pipe{};
+  pipe.start(ws.stage0, ws.bar0, warp_global(), warp_count(), T.tiles, lane, issue);
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     if (!pipe.wait()) break;
     Rows v;
     tile_read_bf16(pipe.cur(), blk, l4, v);
-    pipe.refill(&xmap, lane);
+    pipe.refill(lane, issue);
     Quant q;
     if (FWHT) {
       level1_fwd(v);
@@ -862,40 +896,75 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 }
 
 // K4: emulated R-way reduce. R payloads -> transform-domain FP32 sum in rank order ->
-// requantised payload (no transform).
-struct RankPtrs {
-  const uint8_t* p[FP4Q_MAX_RANKS];
+// requantised payload (no transform). Each rank's tile (1024 code bytes, 128 or 64
+// group-scale bytes, 32 block-scale bytes) arrives by TMA into a per-warp stage.
+constexpr int kRankStageBytes = 1024 + 128 + 128;   // codes | group scales | block scales
+
+struct RankMaps {
+  CUtensorMap codes[FP4Q_MAX_RANKS];   // [nb][128] bytes, box [128, 8]
+  CUtensorMap gsc[FP4Q_MAX_RANKS];     // G=16: [nb][16] box [16, 8]; G=32: [nb/2][16] box [16, 4]
+  CUtensorMap bsc[FP4Q_MAX_RANKS];     // [nb] floats, box [8]
 };
 
-template <int G>
+template <int R>
+struct ReduceCfg {
+  static constexpr int kStagesR = R <= 4 ? 3 : 2;
+  static constexpr int kStageBytes = R * kRankStageBytes;
+  static constexpr int kRegion = kStagesR * kStageBytes + 128;       // + barriers
+  static constexpr int kCtaBytes = kCtaWarps * kRegion + 128;
+};
+
+template <int G, int R>
 __global__ void __launch_bounds__(kCtaWarps * 32)
-reduce_kernel(RankPtrs in, int R, int64_t n, Payload out, TileLoop T) {
-  const int lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  for (int64_t t = warp_global(); t < T.tiles; t += warp_count()) {
+reduce_kernel(const __grid_constant__ RankMaps maps, Payload out, TileLoop T) {
+  typedef ReduceCfg<R> C;
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
+  const uint32_t base = ((smem_addr(smem_raw) + 127u) & ~127u) + (uint32_t)(warp * C::kRegion);
+  constexpr uint32_t gs_bytes = G == 16 ? 128 : 64;
+  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
+    mbar_expect_tx(bar, (uint32_t)R * (1024u + gs_bytes + 32u));
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const uint32_t b = buf + (uint32_t)(r * kRankStageBytes);
+      tma_load_2d(b, &maps.codes[r], 0, (int32_t)(t * kTileBlocks), bar);
+      tma_load_2d(b + 1024, &maps.gsc[r], 0, (int32_t)(t * (G == 16 ? kTileBlocks : kTileBlocks / 2)), bar);
+      tma_load_1d(b + 1152, &maps.bsc[r], (int32_t)(t * kTileBlocks), bar);
+    }
+  };
+  InPipe<C::kStagesR, C::kStageBytes> pipe{};
+  pipe.start(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), warp_global(), warp_count(), T.tiles,
+             lane, issue);
+  for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     const int64_t gb = t * kTileBlocks + blk;
     const bool valid = gb < T.nb;
+    if (!pipe.wait()) return;
     Rows z;
-    if (valid) {
-      PayRaw raw;
-      float S[4];
-      pay_load<G, false>(payload_of(const_cast<uint8_t*>(in.p[0]), n, G), gb, l4, raw);
-      pay_scales<G, false>(raw, l4, S);
-      dequantize(raw.code, S, z);
 #pragma unroll
-      for (int r = 1; r < FP4Q_MAX_RANKS; ++r) {
-        if (r >= R) break;
+    for (int r = 0; r < R; ++r) {
+      const uint32_t b = pipe.cur() + (uint32_t)(r * kRankStageBytes);
+      PayRaw raw;
+      const uint4 c0 = lds128(b + (uint32_t)(blk * 128 + l4 * 32));
+      const uint4 c1 = lds128(b + (uint32_t)(blk * 128 + l4 * 32 + 16));
+      raw.code[0][0] = c0.x; raw.code[0][1] = c0.y; raw.code[1][0] = c0.z; raw.code[1][1] = c0.w;
+      raw.code[2][0] = c1.x; raw.code[2][1] = c1.y; raw.code[3][0] = c1.z; raw.code[3][1] = c1.w;
+      raw.g[0] = G == 16 ? lds32(b + 1024u + (uint32_t)(blk * 16 + 4 * l4))
+                         : lds16(b + 1024u + (uint32_t)(blk * 8 + 2 * l4));
+      raw.sb = __uint_as_float(lds32(b + 1152u + (uint32_t)(4 * blk)));
+      float S[4];
+      pay_scales<G, false>(raw, l4, S);
+      if (r == 0) {
+        dequantize(raw.code, S, z);
+      } else {
         Rows xr;
-        pay_load<G, false>(payload_of(const_cast<uint8_t*>(in.p[r]), n, G), gb, l4, raw);
-        pay_scales<G, false>(raw, l4, S);
         dequantize(raw.code, S, xr);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
           for (int j = 0; j < 8; ++j) z[k][j] = add2(z[k][j], xr[k][j]);
       }
-    } else {
-      zero_rows(z);
     }
+    pipe.refill(lane, issue);
     Quant q;
     quantize<G, false, false>(z, q);
     if (valid) store_block<G, false>(out, gb, l4, q);
@@ -1055,15 +1124,73 @@ fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) 
   return launched();
 }
 
-template <int G>
-fp4q_status launch_reduce(const RankPtrs& in, int R, int64_t n, void* out, cudaStream_t s) {
+// Tensor maps over one payload's three segments for the reduce's per-tile boxes.
+bool payload_maps(RankMaps& m, int r, const void* base, int64_t n, int G) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  const uint8_t* p = static_cast<const uint8_t*>(base);
+  const int64_t nb = n / FP4Q_BLOCK;
+  const cuuint32_t estr[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {128, (cuuint64_t)nb};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, (cuuint32_t)kTileBlocks};
+    if (enc(&m.codes[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    // G = 32: two blocks' 8 scale bytes per 16-byte row (the segment is padded to 16 bytes)
+    const cuuint64_t rows = G == 16 ? (cuuint64_t)nb : (cuuint64_t)((nb + 1) / 2);
+    const cuuint64_t dims[2] = {16, rows};
+    const cuuint64_t strides[1] = {16};
+    const cuuint32_t box[2] = {16, (cuuint32_t)(G == 16 ? kTileBlocks : kTileBlocks / 2)};
+    if (enc(&m.gsc[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p + n / 2), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    // rank 1: the driver rejects a null stride array even though it has no entries to read
+    const cuuint64_t dims[1] = {(cuuint64_t)nb};
+    const cuuint64_t unused_strides[1] = {16};
+    const cuuint32_t box[1] = {(cuuint32_t)kTileBlocks};
+    if (enc(&m.bsc[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<uint8_t*>(p + n / 2 + pad16(n / G)), dims,
+            unused_strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
+template <int G, int R>
+fp4q_status launch_reduce_r(const RankMaps& maps, int64_t n, void* out, cudaStream_t s) {
   TileLoop T = tiles_of(n);
-  auto k = reduce_kernel<G>;
+  auto k = reduce_kernel<G, R>;
   Launch L;
-  fp4q_status st = plan(k, 0, T.tiles, L);
+  fp4q_status st = plan(k, ReduceCfg<R>::kCtaBytes, T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kCtaWarps * 32, 0, s>>>(in, R, n, payload_of(out, n, G), T);
+  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(maps, payload_of(out, n, G), T);
   return launched();
+}
+
+template <int G>
+fp4q_status launch_reduce(const void* const* payloads, int R, int64_t n, void* out, cudaStream_t s) {
+  RankMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  for (int r = 0; r < R; ++r)
+    if (!payload_maps(maps, r, payloads[r], n, G)) return FP4Q_ERR_CUDA;
+  switch (R) {
+    case 1: return launch_reduce_r<G, 1>(maps, n, out, s);
+    case 2: return launch_reduce_r<G, 2>(maps, n, out, s);
+    case 3: return launch_reduce_r<G, 3>(maps, n, out, s);
+    case 4: return launch_reduce_r<G, 4>(maps, n, out, s);
+    case 5: return launch_reduce_r<G, 5>(maps, n, out, s);
+    case 6: return launch_reduce_r<G, 6>(maps, n, out, s);
+    case 7: return launch_reduce_r<G, 7>(maps, n, out, s);
+    default: return launch_reduce_r<G, 8>(maps, n, out, s);
+  }
 }
 
 size_t payload_bytes_of(int64_t n, int G) {
@@ -1169,10 +1296,8 @@ fp4q_status fp4q_reduce_requantize(const void* const* payloads, int32_t R, int64
   const size_t pb = payload_bytes_of(n, G);
   for (int r = 0; r < R; ++r)
     if (overlap(payloads[r], pb, out_payload, pb)) return FP4Q_ERR_OVERLAP;
-  RankPtrs in;
-  for (int r = 0; r < FP4Q_MAX_RANKS; ++r) in.p[r] = r < R ? static_cast<const uint8_t*>(payloads[r]) : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return G == 16 ? launch_reduce<16>(in, R, n, out_payload, s) : launch_reduce<32>(in, R, n, out_payload, s);
+  return G == 16 ? launch_reduce<16>(payloads, R, n, out_payload, s) : launch_reduce<32>(payloads, R, n, out_payload, s);
 }
 
 fp4q_status fp4q_fault_flags(uint32_t* flags, int32_t clear) {
