@@ -44,7 +44,9 @@ class Params(ctypes.Structure):
 
 def build(force: bool = False, nvcc: str = "nvcc") -> str:
     """Compile csrc/fp4q.cu for sm_103a into the package directory; returns the .so path."""
-    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    csrc = os.path.dirname(_SRC)
+    deps = [_HDR] + [os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh"))]
+    newest = max(os.path.getmtime(f) for f in deps)
     if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
         return LIB_PATH
     tmp = LIB_PATH + f".tmp{os.getpid()}"

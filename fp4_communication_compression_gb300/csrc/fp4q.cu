@@ -20,9 +20,11 @@
 // 4 lanes of a block with two xor-shuffles.
 //
 // Exactness. Every floating-point step is a separately rounded FP32 operation: the file is
-// built with -fmad=false, divisions and reciprocals are the IEEE-rounded __fdiv_rn and
-// __frcp_rn, packed ops carry .rn, and no operation is reassociated. Two rewrites are
-// bit-identical to the contract's literal order and are used to save work:
+// built with -fmad=false, packed ops carry .rn, no operation is reassociated, and the scale
+// chain's divisions and reciprocals are the correctly rounded, branch-free FMA refinements of
+// fp4q_math.cuh (checked exhaustively against CUDA's IEEE __fdiv_rn / __frcp_rn over the
+// operand ranges used here). Two rewrites are bit-identical to the contract's literal order
+// and are used to save work:
 //   * compress never multiplies y by 1/16: max|y| = fl(max|z| / 16) because rounding is
 //     monotone, and q = y * inv = z * (inv / 16) exactly whenever a code can depend on it
 //     (inv / 16 is exact for |x| < 2^120; a y that underflows gives |q| < 2^-17, code +-0
@@ -36,6 +38,7 @@
 #include <string.h>
 
 #include "fp4q.h"
+#include "fp4q_math.cuh"
 
 namespace {
 
@@ -69,6 +72,15 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
       "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\t"
       "mul.rn.f32x2 C, A, B;\n\tmov.b64 {%0, %1}, C;}"
       : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+// a * b + c on two pairs at once (one rounding each).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{.reg .b64 A, B, C, D;\n\t"
+      "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\tmov.b64 C, {%6, %7};\n\t"
+      "fma.rn.f32x2 D, A, B, C;\n\tmov.b64 {%0, %1}, D;}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return r;
 }
 // (a, b) <- (a + b, a - b) on two pairs at once.
@@ -150,12 +162,11 @@ __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t codes16) {
 // Rows of one lane: v[k][j] = pair j (positions 2j, 2j+1) of the lane's k-th row.
 typedef float2 Rows[4][8];
 
-// Level 1 (strides 1, 2, 4, 8 inside each row), forward order.
-__device__ __forceinline__ void level1_fwd(Rows v) {
+// Level 1 strides 2, 4, 8 inside each row, forward order (stride 1 is done while the
+// bfloat16 pairs are widened, see bf16x2_bfly).
+__device__ __forceinline__ void level1_fwd_from2(Rows v) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) bfly_in(v[k][j]);
 #pragma unroll
     for (int h = 1; h < 8; h <<= 1)
 #pragma unroll
@@ -263,12 +274,16 @@ __device__ __forceinline__ void quantize(const Rows v, Quant& o) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) am[k] = __fmul_rn(am[k], 0.0625f);
   }
+  // s_b = RN(A / 2688), r = RN(amax / t_b) and inv = RN(1 / S) with the branch-free
+  // correctly rounded division and reciprocal of fp4q_math.cuh (one reciprocal of t_b per
+  // lane serves its four group ratios)
   const bool zero = !(A >= kZeroLimit);
-  const float sb = zero ? 0.0f : __fdiv_rn(A, 2688.0f);
+  const float sb = zero ? 0.0f : fp4q_math::div_rn_2688(A);
   const float tb = zero ? 1.0f : __fmul_rn(sb, 6.0f);
+  const fp4q_math::Divider by_tb(tb);
   float r[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) r[k] = __fdiv_rn(am[k], tb);
+  for (int k = 0; k < 4; ++k) r[k] = by_tb.div(am[k]);
   uint32_t c01 = e4m3x2(r[0], r[1]), c23 = e4m3x2(r[2], r[3]);
   if (zero) c01 = c23 = 0u;
   const float2 s01 = e4m3x2_to_f2(c01), s23 = e4m3x2_to_f2(c23);
@@ -279,7 +294,7 @@ __device__ __forceinline__ void quantize(const Rows v, Quant& o) {
   for (int k = 0; k < 4; ++k) {
     const float S = __fmul_rn(sgv[k], sb);
     o.S[k] = S;
-    float inv = S > 0.0f ? __frcp_rn(S) : 0.0f;
+    float inv = S > 0.0f ? fp4q_math::rcp_rn(S) : 0.0f;
     if (FOLD) inv = __fmul_rn(inv, 0.0625f);
     const float2 iv = make_float2(inv, inv);
     uint32_t w0 = e2m1_pack8(mul2(v[k][0], iv), mul2(v[k][1], iv), mul2(v[k][2], iv), mul2(v[k][3], iv));
@@ -291,34 +306,36 @@ __device__ __forceinline__ void quantize(const Rows v, Quant& o) {
 }
 
 // Decode the lane's 4 rows from codes and per-row scales: x~ = grid(code) * S.
-// The products use the IEEE __fmul_rn, which is never contracted: a packed mul.rn.f32x2
-// whose result feeds a packed add was observed to be fused into an FMA by the toolchain
-// (even with .rn and --fmad=false), which breaks bit parity in the sums that follow.
-__device__ __forceinline__ void dequantize(const uint32_t code[4][2], const float S[4], Rows v) {
+// A packed mul.rn.f32x2 whose product feeds a packed add was observed to be fused into an
+// FMA by the toolchain (even with .rn and --fmad=false), which breaks bit parity in the sums
+// that follow. The products are therefore formed as fma.rn.f32x2(g, S, nz) with nz = -0.0
+// passed in from the host: a * b + (-0) is exactly RN(a * b) (signed zeros included), and an
+// FMA cannot absorb the addition that follows.
+__device__ __forceinline__ void dequantize(const uint32_t code[4][2], const float S[4], Rows v, float nz) {
+  const float2 z2 = make_float2(nz, nz);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
+    const float2 s = make_float2(S[k], S[k]);
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
       float2 g[4];
       e2m1_word_to_f2(code[k][w], g);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        v[k][4 * w + i] = make_float2(__fmul_rn(g[i].x, S[k]), __fmul_rn(g[i].y, S[k]));
+      for (int i = 0; i < 4; ++i) v[k][4 * w + i] = fma2(g[i], s, z2);
     }
   }
 }
 
-// x^ = v / 16. A packed multiply is kept only where the product feeds a conversion or a
-// store; before an accumulation the IEEE scalar multiply is used (see dequantize).
+// x^ = v / 16 (exact unless the result is subnormal). Before an accumulation the product is
+// an FMA with the opaque -0 addend (see dequantize); before a conversion a plain packed
+// multiply is used.
 template <bool BEFORE_ADD>
-__device__ __forceinline__ void scale16(Rows v) {
-  const float2 s16 = make_float2(0.0625f, 0.0625f);
+__device__ __forceinline__ void scale16(Rows v, float nz) {
+  const float2 s16 = make_float2(0.0625f, 0.0625f), z2 = make_float2(nz, nz);
 #pragma unroll
   for (int k = 0; k < 4; ++k)
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      v[k][j] = BEFORE_ADD ? make_float2(__fmul_rn(v[k][j].x, 0.0625f), __fmul_rn(v[k][j].y, 0.0625f))
-                           : mul2(v[k][j], s16);
+    for (int j = 0; j < 8; ++j) v[k][j] = BEFORE_ADD ? fma2(v[k][j], s16, z2) : mul2(v[k][j], s16);
 }
 
 // ------------------------------------------------------------------ payload addressing
@@ -678,6 +695,29 @@ __device__ __forceinline__ void tile_read_bf16(uint32_t buf, int blk, int a, Row
     v[k][j + 3] = bf16x2_to_f2(t.w);
   }
 }
+// bfloat16 pair (x0 low, x1 high) -> (x0 + x1, x0 - x1): the stride-1 butterfly fused with
+// the widening, by the mixed-precision add/sub (bf16 operand widened exactly, one rounding).
+__device__ __forceinline__ float2 bf16x2_bfly(uint32_t w) {
+  float s, d;
+  const float hi = __uint_as_float(w & 0xffff0000u);
+  asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, l, %3;}"
+      : "=f"(s), "=f"(d) : "r"(w), "f"(hi));
+  return make_float2(s, d);
+}
+// As tile_read_bf16, with the stride-1 butterfly applied to every pair.
+__device__ __forceinline__ void tile_read_bf16_bfly(uint32_t buf, int blk, int a, Rows v) {
+  const int line = 4 * blk + a;
+  const uint32_t base = buf + (uint32_t)line * 128u, sw = (uint32_t)(line & 7);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 t = lds128(base + ((((uint32_t)c) ^ sw) << 4));
+    const int k = c >> 1, j = 4 * (c & 1);
+    v[k][j + 0] = bf16x2_bfly(t.x);
+    v[k][j + 1] = bf16x2_bfly(t.y);
+    v[k][j + 2] = bf16x2_bfly(t.z);
+    v[k][j + 3] = bf16x2_bfly(t.w);
+  }
+}
 __device__ __forceinline__ void tile_write_bf16(uint32_t buf, int blk, int a, const Rows v) {
   const int line = 4 * blk + a;
   const uint32_t base = buf + (uint32_t)line * 128u, sw = (uint32_t)(line & 7);
@@ -723,6 +763,7 @@ __device__ __forceinline__ void tile_write_f32(uint32_t buf, int blk, int a, con
 struct TileLoop {
   int64_t tiles;     // number of 8-block tiles
   int64_t nb;        // number of 256-element blocks
+  float negzero;     // -0.0f, set by the host so the compiler cannot see its value
 };
 
 __device__ __forceinline__ int64_t warp_global() {
@@ -765,11 +806,11 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
     const bool valid = gb < T.nb;
     if (!pipe.wait()) return;
     Rows v;
-    tile_read_bf16(pipe.cur(), blk, l4, v);
+    if (FWHT) tile_read_bf16_bfly(pipe.cur(), blk, l4, v); else tile_read_bf16(pipe.cur(), blk, l4, v);
     pipe.refill(lane, issue);
     Quant q;
     if (FWHT) {
-      level1_fwd(v);
+      level1_fwd_from2(v);
       rows_bfly(v, 1);             // h = 16
       rows_bfly(v, 2);             // h = 32
       transpose<true>(v, tbuf, blk, l4);
@@ -813,7 +854,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
     float S[4];
     pay_scales<G, LB>(cur, l4, S);
     Rows v;
-    dequantize(cur.code, S, v);
+    dequantize(cur.code, S, v, T.negzero);
     staging_free(lane);
     if (FWHT) {
       rows_bfly(v, 2);             // h = 128
@@ -822,7 +863,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
       rows_bfly(v, 2);             // h = 32
       rows_bfly(v, 1);             // h = 16
       level1_inv(v);
-      scale16<BETA != 0>(v);
+      scale16<BETA != 0>(v, T.negzero);
     }
     if (BETA) {
       if (!pipe.wait()) break;
@@ -864,11 +905,11 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     if (!pipe.wait()) break;
     Rows v;
-    tile_read_bf16(pipe.cur(), blk, l4, v);
+    if (FWHT) tile_read_bf16_bfly(pipe.cur(), blk, l4, v); else tile_read_bf16(pipe.cur(), blk, l4, v);
     pipe.refill(lane, issue);
     Quant q;
     if (FWHT) {
-      level1_fwd(v);
+      level1_fwd_from2(v);
       rows_bfly(v, 1);
       rows_bfly(v, 2);
       staging_free(lane);
@@ -876,17 +917,17 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       rows_bfly(v, 1);
       rows_bfly(v, 2);
       quantize<G, true, true>(v, q);
-      dequantize(q.code, q.S, v);
+      dequantize(q.code, q.S, v, T.negzero);
       rows_bfly(v, 2);
       rows_bfly(v, 1);
       transpose<false>(v, tbuf, blk, l4);
       rows_bfly(v, 2);
       rows_bfly(v, 1);
       level1_inv(v);
-      scale16<false>(v);
+      scale16<false>(v, T.negzero);
     } else {
       quantize<G, false, false>(v, q);
-      dequantize(q.code, q.S, v);
+      dequantize(q.code, q.S, v, T.negzero);
       staging_free(lane);
     }
     tile_write_bf16(ws.xbuf, blk, l4, v);
@@ -954,10 +995,10 @@ reduce_kernel(const __grid_constant__ RankMaps maps, Payload out, TileLoop T) {
       float S[4];
       pay_scales<G, false>(raw, l4, S);
       if (r == 0) {
-        dequantize(raw.code, S, z);
+        dequantize(raw.code, S, z, T.negzero);
       } else {
         Rows xr;
-        dequantize(raw.code, S, xr);
+        dequantize(raw.code, S, xr, T.negzero);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
@@ -1081,6 +1122,7 @@ TileLoop tiles_of(int64_t n) {
   TileLoop T;
   T.nb = n / FP4Q_BLOCK;
   T.tiles = (T.nb + kTileBlocks - 1) / kTileBlocks;
+  T.negzero = -0.0f;
   return T;
 }
 
