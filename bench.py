@@ -74,11 +74,20 @@ def measured_peak():
         return 6800.0, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
+def kernel_source_sha() -> str:
+    """Hash of everything the kernels are built from (csrc/*.cu, csrc/*.cuh, include/fp4q.h)."""
+    csrc = os.path.join(ROOT, "fp4_communication_compression_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
+    h = hashlib.sha256()
+    for f in files + [os.path.join(ROOT, "include", "fp4q.h")]:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic(kernel: str):
     """DRAM bytes per launch of a kernel from the committed ncu summary, or None when the
     summary is missing or was taken on a different kernel source."""
-    src = os.path.join(ROOT, "fp4_communication_compression_gb300", "csrc", "fp4q.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha()
     for name in sorted(os.listdir(os.path.join(ROOT, "profiles"))) if os.path.isdir(os.path.join(ROOT, "profiles")) else []:
         if not name.endswith(".md"):
             continue
@@ -141,6 +150,19 @@ class ClockSampler:
     def __exit__(self, *exc):
         if self.proc is not None and self.proc.poll() is None:
             self.proc.kill()
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (the slowest rank's time)."""
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time (GB/s)."""
+    return world * bytes_per_rank_step * steps / (max_ms * 1e-3) / 1e9
 
 
 def make_inputs():
@@ -303,12 +325,10 @@ def main():
             per_kernel[name].append(ev[i].elapsed_time(ev[i + 1]))
     dev_ms = float(sum(step_ms))
     if pg:
-        t = torch.tensor([dev_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        dev_ms = float(t.item())
+        dev_ms = max_over_ranks(dev_ms, pg, dev)
     ms_per_step = dev_ms / args.steps
     bytes_in = R_RANKS * 2 * n
-    value = world * bytes_in * args.steps / (dev_ms * 1e-3) / 1e9
+    value = job_gbs(bytes_in, args.steps, world, dev_ms)
 
     peak, peak_src = measured_peak()
     kern = {}
@@ -362,6 +382,7 @@ def main():
         "e2e": {"value": round(world * bytes_in / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "wall_ms_timed_region": round((t1 - t0) * 1e3, 2),
+        "kernel_source_sha256": kernel_source_sha(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(xs_np, resid_np)

@@ -1,0 +1,97 @@
+"""Per-kernel micro-benchmark of the codec on one GPU.
+
+    python -m fp4_communication_compression_gb300.perf [--sizes 16777216 268435456]
+        [--kernels compress decompress_bf16_b1 ...] [--iters 30]
+
+Each kernel is timed alone with CUDA events on the launching stream, after an L2 flush
+(a write of a buffer larger than L2 followed by a read of another one), and reported as
+algorithmic GB/s (the bytes the kernel must move, G = 16) and as a fraction of the measured
+HBM copy bandwidth in MEASURED_PEAKS.json when that file is present. Inputs are N(0,1)
+bfloat16 tensors made on the device (timing only; parity is the tests' business).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+
+import numpy as np
+import torch
+
+import fp4_communication_compression_gb300 as fq
+
+PAYLOAD = 0.5 + 1 / 16 + 4 / 256          # bytes per element of a G = 16 payload
+ALG_BYTES = {
+    "compress": 2 + PAYLOAD,
+    "decompress_bf16_b1": PAYLOAD + 4,
+    "decompress_bf16_b0": PAYLOAD + 2,
+    "decompress_f32_b1": PAYLOAD + 8,
+    "roundtrip": 4.0,
+    "reduce_r2": 3 * PAYLOAD,
+    "reduce_r4": 5 * PAYLOAD,
+    "reduce_r8": 9 * PAYLOAD,
+    "copy_bf16": 4.0,
+}
+
+
+def peak_gbs():
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(path))["hbm_gbs"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--sizes", type=int, nargs="+", default=[1 << 24, 1 << 26, 1 << 28])
+    ap.add_argument("--kernels", nargs="+", default=list(ALG_BYTES))
+    ap.add_argument("--iters", type=int, default=30)
+    args = ap.parse_args()
+    dev = torch.device("cuda:0")
+    peak = peak_gbs()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(args.iters + 3):
+            flush.zero_()
+            clean.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize(dev)
+            if i >= 3:
+                ts.append(a.elapsed_time(b) * 1e-3)
+        return float(np.mean(ts))
+
+    for n in args.sizes:
+        x = torch.randn(n, device=dev).to(torch.bfloat16)
+        ps = [fq.compress(x * (r + 1)) for r in range(8)]
+        d16 = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+        d32 = torch.zeros(n, dtype=torch.float32, device=dev)
+        y = torch.empty_like(x)
+        out = torch.empty_like(ps[0])
+        fns = {
+            "compress": lambda: fq.compress(x, payload=ps[0]),
+            "decompress_bf16_b1": lambda: fq.decompress_accumulate(ps[0], n, d16, beta=1),
+            "decompress_bf16_b0": lambda: fq.decompress_accumulate(ps[0], n, d16, beta=0),
+            "decompress_f32_b1": lambda: fq.decompress_accumulate(ps[0], n, d32, beta=1),
+            "roundtrip": lambda: fq.roundtrip(x, y=y),
+            "reduce_r2": lambda: fq.reduce_requantize(ps[:2], n, out=out),
+            "reduce_r4": lambda: fq.reduce_requantize(ps[:4], n, out=out),
+            "reduce_r8": lambda: fq.reduce_requantize(ps[:8], n, out=out),
+            "copy_bf16": lambda: y.copy_(x),
+        }
+        for k in args.kernels:
+            t = timed(fns[k])
+            gbs = ALG_BYTES[k] * n / t / 1e9
+            print(json.dumps({"n": n, "kernel": k, "us": round(t * 1e6, 2), "alg_gbs": round(gbs, 1),
+                              "frac_of_peak": None if not peak else round(gbs / peak, 4)}), flush=True)
+        del x, ps, d16, d32, y, out
+
+
+if __name__ == "__main__":
+    main()
