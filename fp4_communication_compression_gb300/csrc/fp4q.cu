@@ -43,7 +43,13 @@
 namespace {
 
 constexpr int kTileBlocks = 8;                  // 256-element blocks per warp tile
-constexpr int kCtaWarps = 4;                    // warps per CTA
+// Warps per CTA and input stages per warp, per kernel (shared memory per warp decides how
+// many warps fit on an SM: compress and roundtrip are issue/latency bound and want the
+// most resident warps; one stage is enough because a tile's compute outlasts its load).
+constexpr int kCompressWarps = 3, kCompressStages = 1;
+constexpr int kRoundtripWarps = 3, kRoundtripStages = 1;
+constexpr int kDecompressWarps = 4, kDecompressStages = 1;
+constexpr int kReduceWarps = 4;
 constexpr int kUnitsPerBlock = 73;              // 16-byte units per block in the transpose buffer
 constexpr float kZeroLimit = 2688.0f * 0x1p-100f;   // all-zero block guard on A_b
 constexpr unsigned kFull = 0xffffffffu;
@@ -527,12 +533,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* map, int32_t c0, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(src)
@@ -580,7 +580,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   return false;
 }
 
-constexpr int kStages = 2;                 // input tiles in flight per warp
 constexpr int kTileLinesBF16 = 32;         // 128-byte lines per 8-block bf16 tile (4 KiB)
 constexpr int kTileLinesF32 = 64;          // 128-byte lines per 8-block f32 tile (8 KiB)
 constexpr int kXBufBytes = 10240;          // transpose buffer / output staging + barriers
@@ -588,10 +587,10 @@ constexpr int kXBufUsed = kUnitsPerBlock * 16 * kTileBlocks;   // 9344 bytes of 
 
 // Per-warp shared memory: [input stages][xbuf], every part 1024-byte aligned (the 128-byte
 // TMA swizzle repeats every 1024 bytes); the stage barriers sit in the xbuf's unused tail.
-template <int IN_BYTES>
+template <int WARPS, int STAGES, int IN_BYTES>
 struct WarpSmemLayout {
-  static constexpr int kRegion = kStages * IN_BYTES + kXBufBytes;
-  static constexpr int kCtaBytes = kCtaWarps * kRegion + 1024;
+  static constexpr int kRegion = STAGES * IN_BYTES + kXBufBytes;
+  static constexpr int kCtaBytes = WARPS * kRegion + 1024;
 };
 
 struct WarpSmem {
@@ -599,14 +598,14 @@ struct WarpSmem {
   uint8_t* xbuf_ptr;
 };
 
-template <int IN_BYTES>
+template <int STAGES, int IN_BYTES>
 __device__ __forceinline__ WarpSmem warp_smem(uint8_t* raw, int warp) {
-  typedef WarpSmemLayout<IN_BYTES> L;
+  constexpr int region = STAGES * IN_BYTES + kXBufBytes;
   const uint32_t raw_s = smem_addr(raw);
-  const uint32_t base = ((raw_s + 1023u) & ~1023u) + (uint32_t)(warp * L::kRegion);
+  const uint32_t base = ((raw_s + 1023u) & ~1023u) + (uint32_t)(warp * region);
   WarpSmem w;
   w.stage0 = base;
-  w.xbuf = base + kStages * IN_BYTES;
+  w.xbuf = base + STAGES * IN_BYTES;
   w.bar0 = w.xbuf + kXBufUsed;
   w.xbuf_ptr = raw + (w.xbuf - raw_s);
   return w;
@@ -766,10 +765,12 @@ struct TileLoop {
   float negzero;     // -0.0f, set by the host so the compiler cannot see its value
 };
 
+template <int WARPS>
 __device__ __forceinline__ int64_t warp_global() {
-  return (int64_t)blockIdx.x * kCtaWarps + (threadIdx.x >> 5);
+  return (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
 }
-__device__ __forceinline__ int64_t warp_count() { return (int64_t)gridDim.x * kCtaWarps; }
+template <int WARPS>
+__device__ __forceinline__ int64_t warp_count() { return (int64_t)gridDim.x * WARPS; }
 
 // Lane 0 of the warp waits until its last TMA store has finished reading the staging buffer.
 __device__ __forceinline__ void staging_free(int lane) {
@@ -789,18 +790,18 @@ __device__ __forceinline__ void staging_store(const CUtensorMap* map, int lines,
 
 // K1: compress. x (bfloat16, n) -> payload. Input tiles arrive by TMA.
 template <int G, int FWHT>
-__global__ void __launch_bounds__(kCtaWarps * 32)
+__global__ void __launch_bounds__(kCompressWarps * 32)
 compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  const WarpSmem ws = warp_smem<4096>(smem_raw, warp);
+  const WarpSmem ws = warp_smem<kCompressStages, 4096>(smem_raw, warp);
   float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
     mbar_expect_tx(bar, 4096);
     tma_load_2d(buf, &xmap, 0, (int32_t)(t * kTileLinesBF16), bar);
   };
-  InPipe<kStages, 4096> pipe{};
-  pipe.start(ws.stage0, ws.bar0, warp_global(), warp_count(), T.tiles, lane, issue);
+  InPipe<kCompressStages, 4096> pipe{};
+  pipe.start(ws.stage0, ws.bar0, warp_global<kCompressWarps>(), warp_count<kCompressWarps>(), T.tiles, lane, issue);
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     const int64_t gb = t * kTileBlocks + blk;
     const bool valid = gb < T.nb;
@@ -829,21 +830,21 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
 // The payload of the next tile is prefetched into registers; dst tiles are read (BETA) and
 // written through the swizzled shared staging buffer by TMA.
 template <int G, int FWHT, int DT, int BETA>
-__global__ void __launch_bounds__(kCtaWarps * 32)
+__global__ void __launch_bounds__(kDecompressWarps * 32)
 decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop T) {
   constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
   constexpr int LINES = DT == FP4Q_BF16 ? kTileLinesBF16 : kTileLinesF32;
   constexpr bool LB = FWHT != 0;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  const WarpSmem ws = warp_smem<BETA ? TB : 0>(smem_raw, warp);
+  const WarpSmem ws = warp_smem<kDecompressStages, BETA ? TB : 0>(smem_raw, warp);
   float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
     mbar_expect_tx(bar, TB);
     tma_load_2d(buf, &dmap, 0, (int32_t)(t * LINES), bar);
   };
-  InPipe<kStages, TB> pipe{};
-  const int64_t t0 = warp_global(), W = warp_count();
+  InPipe<kDecompressStages, TB> pipe{};
+  const int64_t t0 = warp_global<kDecompressWarps>(), W = warp_count<kDecompressWarps>();
   if (BETA) pipe.start(ws.stage0, ws.bar0, t0, W, T.tiles, lane, issue);
   PayRaw cur, nxt;
   if (t0 < T.tiles && t0 * kTileBlocks + blk < T.nb) pay_load<G, LB>(P, t0 * kTileBlocks + blk, l4, cur);
@@ -890,18 +891,19 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
 
 // K3: fused roundtrip. x (bfloat16) -> y = bf16(decode(compress(x))), no payload.
 template <int G, int FWHT>
-__global__ void __launch_bounds__(kCtaWarps * 32)
+__global__ void __launch_bounds__(kRoundtripWarps * 32)
 roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap, TileLoop T) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  const WarpSmem ws = warp_smem<4096>(smem_raw, warp);
+  const WarpSmem ws = warp_smem<kRoundtripStages, 4096>(smem_raw, warp);
   float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
     mbar_expect_tx(bar, 4096);
     tma_load_2d(buf, &xmap, 0, (int32_t)(t * kTileLinesBF16), bar);
   };
-  InPipe<kStages, 4096> pipe{};
-  pipe.start(ws.stage0, ws.bar0, warp_global(), warp_count(), T.tiles, lane, issue);
+  InPipe<kRoundtripStages, 4096> pipe{};
+  pipe.start(ws.stage0, ws.bar0, warp_global<kRoundtripWarps>(), warp_count<kRoundtripWarps>(), T.tiles, lane,
+             issue);
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     if (!pipe.wait()) break;
     Rows v;
@@ -937,48 +939,67 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 }
 
 // K4: emulated R-way reduce. R payloads -> transform-domain FP32 sum in rank order ->
-// requantised payload (no transform). Each rank's tile (1024 code bytes, 128 or 64
-// group-scale bytes, 32 block-scale bytes) arrives by TMA into a per-warp stage.
-constexpr int kRankStageBytes = 1024 + 128 + 128;   // codes | group scales | block scales
+// requantised payload (no transform). Each rank's tile of codes (1 KiB) and group scales
+// (128 or 64 bytes) is contiguous in its payload and arrives by one plain bulk copy each
+// (exact byte counts for the last, partial tile); block scales are read with one load per
+// lane, one tile ahead.
+constexpr int kRankStageBytes = 1024 + 128;   // codes | group scales
 
-struct RankMaps {
-  CUtensorMap codes[FP4Q_MAX_RANKS];   // [nb][128] bytes, box [128, 8]
-  CUtensorMap gsc[FP4Q_MAX_RANKS];     // G=16: [nb][16] box [16, 8]; G=32: [nb/2][16] box [16, 4]
-  CUtensorMap bsc[FP4Q_MAX_RANKS];     // [nb] floats, box [8]
+struct RankPtrs {
+  const uint8_t* codes[FP4Q_MAX_RANKS];
+  const uint8_t* gsc[FP4Q_MAX_RANKS];
+  const float* bsc[FP4Q_MAX_RANKS];
 };
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
 template <int R>
 struct ReduceCfg {
   static constexpr int kStagesR = R <= 4 ? 3 : 2;
   static constexpr int kStageBytes = R * kRankStageBytes;
   static constexpr int kRegion = kStagesR * kStageBytes + 128;       // + barriers
-  static constexpr int kCtaBytes = kCtaWarps * kRegion + 128;
+  static constexpr int kCtaBytes = kReduceWarps * kRegion + 128;
 };
 
 template <int G, int R>
-__global__ void __launch_bounds__(kCtaWarps * 32)
-reduce_kernel(const __grid_constant__ RankMaps maps, Payload out, TileLoop T) {
+__global__ void __launch_bounds__(kReduceWarps * 32)
+reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
   typedef ReduceCfg<R> C;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const uint32_t base = ((smem_addr(smem_raw) + 127u) & ~127u) + (uint32_t)(warp * C::kRegion);
-  constexpr uint32_t gs_bytes = G == 16 ? 128 : 64;
+  constexpr uint32_t gs_per_block = G == 16 ? 16 : 8;
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
-    mbar_expect_tx(bar, (uint32_t)R * (1024u + gs_bytes + 32u));
+    const int64_t left = T.nb - t * kTileBlocks;
+    const uint32_t nblk = (uint32_t)(left < kTileBlocks ? left : kTileBlocks);
+    const uint32_t cbytes = nblk * 128u, gbytes = (nblk * gs_per_block + 15u) & ~15u;
+    mbar_expect_tx(bar, (uint32_t)R * (cbytes + gbytes));
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const uint32_t b = buf + (uint32_t)(r * kRankStageBytes);
-      tma_load_2d(b, &maps.codes[r], 0, (int32_t)(t * kTileBlocks), bar);
-      tma_load_2d(b + 1024, &maps.gsc[r], 0, (int32_t)(t * (G == 16 ? kTileBlocks : kTileBlocks / 2)), bar);
-      tma_load_1d(b + 1152, &maps.bsc[r], (int32_t)(t * kTileBlocks), bar);
+      bulk_load(b, in.codes[r] + t * 1024, cbytes, bar);
+      bulk_load(b + 1024, in.gsc[r] + t * (kTileBlocks * gs_per_block), gbytes, bar);
     }
   };
   InPipe<C::kStagesR, C::kStageBytes> pipe{};
-  pipe.start(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), warp_global(), warp_count(), T.tiles,
-             lane, issue);
+  pipe.start(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), warp_global<kReduceWarps>(),
+             warp_count<kReduceWarps>(), T.tiles, lane, issue);
+  float sb_cur[R], sb_nxt[R];
+  {
+    const int64_t gb = pipe.t0 * kTileBlocks + blk;
+#pragma unroll
+    for (int r = 0; r < R; ++r) sb_cur[r] = (pipe.t0 < T.tiles && gb < T.nb) ? __ldg(in.bsc[r] + gb) : 0.0f;
+  }
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     const int64_t gb = t * kTileBlocks + blk;
     const bool valid = gb < T.nb;
+    const int64_t gbn = gb + pipe.W * kTileBlocks;
+#pragma unroll
+    for (int r = 0; r < R; ++r) sb_nxt[r] = gbn < T.nb ? __ldg(in.bsc[r] + gbn) : 0.0f;
     if (!pipe.wait()) return;
     Rows z;
 #pragma unroll
@@ -991,7 +1012,7 @@ reduce_kernel(const __grid_constant__ RankMaps maps, Payload out, TileLoop T) {
       raw.code[2][0] = c1.x; raw.code[2][1] = c1.y; raw.code[3][0] = c1.z; raw.code[3][1] = c1.w;
       raw.g[0] = G == 16 ? lds32(b + 1024u + (uint32_t)(blk * 16 + 4 * l4))
                          : lds16(b + 1024u + (uint32_t)(blk * 8 + 2 * l4));
-      raw.sb = __uint_as_float(lds32(b + 1152u + (uint32_t)(4 * blk)));
+      raw.sb = sb_cur[r];
       float S[4];
       pay_scales<G, false>(raw, l4, S);
       if (r == 0) {
@@ -1009,6 +1030,8 @@ reduce_kernel(const __grid_constant__ RankMaps maps, Payload out, TileLoop T) {
     Quant q;
     quantize<G, false, false>(z, q);
     if (valid) store_block<G, false>(out, gb, l4, q);
+#pragma unroll
+    for (int r = 0; r < R; ++r) sb_cur[r] = sb_nxt[r];
   }
 }
 
@@ -1048,17 +1071,17 @@ struct Launch {
 
 // Persistent grid: as many CTAs as fit on all SMs at once, never more than the tiles need.
 template <typename K>
-fp4q_status plan(K kernel, int smem, int64_t tiles, Launch& L) {
+fp4q_status plan(K kernel, int warps, int smem, int64_t tiles, Launch& L) {
   const int sms = num_sms();
   if (sms <= 0) return FP4Q_ERR_CUDA;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return FP4Q_ERR_CUDA;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kCtaWarps * 32, smem) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, warps * 32, smem) != cudaSuccess ||
       per_sm <= 0)
     return FP4Q_ERR_CUDA;
-  const int64_t want = (tiles + kCtaWarps - 1) / kCtaWarps;
+  const int64_t want = (tiles + warps - 1) / warps;
   const int64_t cap = (int64_t)per_sm * sms;
   L.grid = (int)(want < cap ? want : cap);
   L.smem = smem;
@@ -1133,9 +1156,10 @@ fp4q_status launch_compress(const void* x, int64_t n, void* payload, cudaStream_
   if (!line_map(&xm, x, n, false)) return FP4Q_ERR_CUDA;
   auto k = compress_kernel<G, F>;
   Launch L;
-  fp4q_status st = plan(k, WarpSmemLayout<4096>::kCtaBytes, T.tiles, L);
+  fp4q_status st = plan(k, kCompressWarps, WarpSmemLayout<kCompressWarps, kCompressStages, 4096>::kCtaBytes,
+                        T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(xm, payload_of(payload, n, G), T);
+  k<<<L.grid, kCompressWarps * 32, L.smem, s>>>(xm, payload_of(payload, n, G), T);
   return launched();
 }
 
@@ -1147,9 +1171,10 @@ fp4q_status launch_decompress(const void* payload, int64_t n, void* dst, cudaStr
   auto k = decompress_kernel<G, F, DT, B>;
   constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
   Launch L;
-  fp4q_status st = plan(k, WarpSmemLayout<B ? TB : 0>::kCtaBytes, T.tiles, L);
+  fp4q_status st = plan(k, kDecompressWarps,
+                        WarpSmemLayout<kDecompressWarps, kDecompressStages, B ? TB : 0>::kCtaBytes, T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(dm, payload_of(const_cast<void*>(payload), n, G), T);
+  k<<<L.grid, kDecompressWarps * 32, L.smem, s>>>(dm, payload_of(const_cast<void*>(payload), n, G), T);
   return launched();
 }
 
@@ -1160,78 +1185,43 @@ fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) 
   if (!line_map(&xm, x, n, false) || !line_map(&ym, y, n, false)) return FP4Q_ERR_CUDA;
   auto k = roundtrip_kernel<G, F>;
   Launch L;
-  fp4q_status st = plan(k, WarpSmemLayout<4096>::kCtaBytes, T.tiles, L);
+  fp4q_status st = plan(k, kRoundtripWarps, WarpSmemLayout<kRoundtripWarps, kRoundtripStages, 4096>::kCtaBytes,
+                        T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(xm, ym, T);
+  k<<<L.grid, kRoundtripWarps * 32, L.smem, s>>>(xm, ym, T);
   return launched();
 }
 
-// Tensor maps over one payload's three segments for the reduce's per-tile boxes.
-bool payload_maps(RankMaps& m, int r, const void* base, int64_t n, int G) {
-  EncodeTiled enc = encode_fn();
-  if (!enc) return false;
-  const uint8_t* p = static_cast<const uint8_t*>(base);
-  const int64_t nb = n / FP4Q_BLOCK;
-  const cuuint32_t estr[2] = {1, 1};
-  {
-    const cuuint64_t dims[2] = {128, (cuuint64_t)nb};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {128, (cuuint32_t)kTileBlocks};
-    if (enc(&m.codes[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
-  }
-  {
-    // G = 32: two blocks' 8 scale bytes per 16-byte row (the segment is padded to 16 bytes)
-    const cuuint64_t rows = G == 16 ? (cuuint64_t)nb : (cuuint64_t)((nb + 1) / 2);
-    const cuuint64_t dims[2] = {16, rows};
-    const cuuint64_t strides[1] = {16};
-    const cuuint32_t box[2] = {16, (cuuint32_t)(G == 16 ? kTileBlocks : kTileBlocks / 2)};
-    if (enc(&m.gsc[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p + n / 2), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
-  }
-  {
-    // rank 1: the driver rejects a null stride array even though it has no entries to read
-    const cuuint64_t dims[1] = {(cuuint64_t)nb};
-    const cuuint64_t unused_strides[1] = {16};
-    const cuuint32_t box[1] = {(cuuint32_t)kTileBlocks};
-    if (enc(&m.bsc[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<uint8_t*>(p + n / 2 + pad16(n / G)), dims,
-            unused_strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
-  }
-  return true;
-}
-
 template <int G, int R>
-fp4q_status launch_reduce_r(const RankMaps& maps, int64_t n, void* out, cudaStream_t s) {
+fp4q_status launch_reduce_r(const RankPtrs& in, int64_t n, void* out, cudaStream_t s) {
   TileLoop T = tiles_of(n);
   auto k = reduce_kernel<G, R>;
   Launch L;
-  fp4q_status st = plan(k, ReduceCfg<R>::kCtaBytes, T.tiles, L);
+  fp4q_status st = plan(k, kReduceWarps, ReduceCfg<R>::kCtaBytes, T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kCtaWarps * 32, L.smem, s>>>(maps, payload_of(out, n, G), T);
+  k<<<L.grid, kReduceWarps * 32, L.smem, s>>>(in, payload_of(out, n, G), T);
   return launched();
 }
 
 template <int G>
 fp4q_status launch_reduce(const void* const* payloads, int R, int64_t n, void* out, cudaStream_t s) {
-  RankMaps maps;
-  memset(&maps, 0, sizeof(maps));
-  for (int r = 0; r < R; ++r)
-    if (!payload_maps(maps, r, payloads[r], n, G)) return FP4Q_ERR_CUDA;
+  RankPtrs in;
+  memset(&in, 0, sizeof(in));
+  for (int r = 0; r < R; ++r) {
+    const Payload p = payload_of(const_cast<void*>(payloads[r]), n, G);
+    in.codes[r] = p.codes;
+    in.gsc[r] = p.gsc;
+    in.bsc[r] = p.bsc;
+  }
   switch (R) {
-    case 1: return launch_reduce_r<G, 1>(maps, n, out, s);
-    case 2: return launch_reduce_r<G, 2>(maps, n, out, s);
-    case 3: return launch_reduce_r<G, 3>(maps, n, out, s);
-    case 4: return launch_reduce_r<G, 4>(maps, n, out, s);
-    case 5: return launch_reduce_r<G, 5>(maps, n, out, s);
-    case 6: return launch_reduce_r<G, 6>(maps, n, out, s);
-    case 7: return launch_reduce_r<G, 7>(maps, n, out, s);
-    default: return launch_reduce_r<G, 8>(maps, n, out, s);
+    case 1: return launch_reduce_r<G, 1>(in, n, out, s);
+    case 2: return launch_reduce_r<G, 2>(in, n, out, s);
+    case 3: return launch_reduce_r<G, 3>(in, n, out, s);
+    case 4: return launch_reduce_r<G, 4>(in, n, out, s);
+    case 5: return launch_reduce_r<G, 5>(in, n, out, s);
+    case 6: return launch_reduce_r<G, 6>(in, n, out, s);
+    case 7: return launch_reduce_r<G, 7>(in, n, out, s);
+    default: return launch_reduce_r<G, 8>(in, n, out, s);
   }
 }
 
