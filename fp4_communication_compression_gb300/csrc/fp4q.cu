@@ -332,16 +332,17 @@ __device__ __forceinline__ void dequantize(const uint32_t code[4][2], const floa
   }
 }
 
-// x^ = v / 16 (exact unless the result is subnormal). Before an accumulation the product is
-// an FMA with the opaque -0 addend (see dequantize); before a conversion a plain packed
-// multiply is used.
-template <bool BEFORE_ADD>
-__device__ __forceinline__ void scale16(Rows v, float nz) {
-  const float2 s16 = make_float2(0.0625f, 0.0625f), z2 = make_float2(nz, nz);
+// The decode's final multiplication by 1/16 is folded into the decode scales: x~/16 =
+// RN(grid * (S/16)) exactly (S/16 is exact, and the product stays normal: S >= 2^-109
+// because a non-zero block has s_b >= 2^-100 and s_g >= 2^-9), and every butterfly of the
+// inverse transform then works on values divided by 16. All of them are multiples of 2^-137
+// (decoded values are normal with ulp >= 2^-133), so each sum is either exact (below 2^-114)
+// or rounded in a binade where scaling by 2^4 commutes with the rounding: the result is
+// bit-identical to transforming x~ and multiplying by 1/16 last. Payloads from compress and
+// reduce always satisfy s_b = 0 or s_b >= 2^-100.
+__device__ __forceinline__ void scale_by_16th(float S[4]) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[k][j] = BEFORE_ADD ? fma2(v[k][j], s16, z2) : mul2(v[k][j], s16);
+  for (int k = 0; k < 4; ++k) S[k] = __fmul_rn(S[k], 0.0625f);
 }
 
 // ------------------------------------------------------------------ payload addressing
@@ -854,6 +855,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
     if (tn < T.tiles && gbn < T.nb) pay_load<G, LB>(P, gbn, l4, nxt); else pay_zero(nxt);
     float S[4];
     pay_scales<G, LB>(cur, l4, S);
+    if (FWHT) scale_by_16th(S);
     Rows v;
     dequantize(cur.code, S, v, T.negzero);
     staging_free(lane);
@@ -864,7 +866,6 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
       rows_bfly(v, 2);             // h = 32
       rows_bfly(v, 1);             // h = 16
       level1_inv(v);
-      scale16<BETA != 0>(v, T.negzero);
     }
     if (BETA) {
       if (!pipe.wait()) break;
@@ -919,6 +920,7 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       rows_bfly(v, 1);
       rows_bfly(v, 2);
       quantize<G, true, true>(v, q);
+      scale_by_16th(q.S);
       dequantize(q.code, q.S, v, T.negzero);
       rows_bfly(v, 2);
       rows_bfly(v, 1);
@@ -926,7 +928,6 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       rows_bfly(v, 2);
       rows_bfly(v, 1);
       level1_inv(v);
-      scale16<false>(v, T.negzero);
     } else {
       quantize<G, false, false>(v, q);
       dequantize(q.code, q.S, v, T.negzero);
@@ -939,11 +940,12 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 }
 
 // K4: emulated R-way reduce. R payloads -> transform-domain FP32 sum in rank order ->
-// requantised payload (no transform). Each rank's tile of codes (1 KiB) and group scales
-// (128 or 64 bytes) is contiguous in its payload and arrives by one plain bulk copy each
-// (exact byte counts for the last, partial tile); block scales are read with one load per
-// lane, one tile ahead.
-constexpr int kRankStageBytes = 1024 + 128;   // codes | group scales
+// requantised payload (no transform). Each rank's tile of codes (1 KiB), group scales (128 or
+// 64 bytes) and block scales (32 bytes) is contiguous in its payload and arrives by plain
+// bulk copies. Their sizes are exact for the last, partial tile (never reading past a
+// payload); the bulk copy moves whole 16-byte units, so up to three block scales of that
+// last tile are read with plain loads instead.
+constexpr int kRankStageBytes = 1024 + 128 + 32;   // codes | group scales | block scales
 
 struct RankPtrs {
   const uint8_t* codes[FP4Q_MAX_RANKS];
@@ -977,29 +979,25 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
     const int64_t left = T.nb - t * kTileBlocks;
     const uint32_t nblk = (uint32_t)(left < kTileBlocks ? left : kTileBlocks);
     const uint32_t cbytes = nblk * 128u, gbytes = (nblk * gs_per_block + 15u) & ~15u;
-    mbar_expect_tx(bar, (uint32_t)R * (cbytes + gbytes));
+    const uint32_t sbytes = (nblk * 4u) & ~15u;
+    mbar_expect_tx(bar, (uint32_t)R * (cbytes + gbytes + sbytes));
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const uint32_t b = buf + (uint32_t)(r * kRankStageBytes);
       bulk_load(b, in.codes[r] + t * 1024, cbytes, bar);
       bulk_load(b + 1024, in.gsc[r] + t * (kTileBlocks * gs_per_block), gbytes, bar);
+      if (sbytes) bulk_load(b + 1152, in.bsc[r] + t * kTileBlocks, sbytes, bar);
     }
   };
   InPipe<C::kStagesR, C::kStageBytes> pipe{};
   pipe.start(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), warp_global<kReduceWarps>(),
              warp_count<kReduceWarps>(), T.tiles, lane, issue);
-  float sb_cur[R], sb_nxt[R];
-  {
-    const int64_t gb = pipe.t0 * kTileBlocks + blk;
-#pragma unroll
-    for (int r = 0; r < R; ++r) sb_cur[r] = (pipe.t0 < T.tiles && gb < T.nb) ? __ldg(in.bsc[r] + gb) : 0.0f;
-  }
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     const int64_t gb = t * kTileBlocks + blk;
     const bool valid = gb < T.nb;
-    const int64_t gbn = gb + pipe.W * kTileBlocks;
-#pragma unroll
-    for (int r = 0; r < R; ++r) sb_nxt[r] = gbn < T.nb ? __ldg(in.bsc[r] + gbn) : 0.0f;
+    // a block scale outside the bulk-copied whole 16-byte units of the last tile
+    const int64_t left = T.nb - t * kTileBlocks;
+    const bool direct_sb = valid && left < kTileBlocks && blk >= (int)(left & ~3);
     if (!pipe.wait()) return;
     Rows z;
 #pragma unroll
@@ -1012,7 +1010,7 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
       raw.code[2][0] = c1.x; raw.code[2][1] = c1.y; raw.code[3][0] = c1.z; raw.code[3][1] = c1.w;
       raw.g[0] = G == 16 ? lds32(b + 1024u + (uint32_t)(blk * 16 + 4 * l4))
                          : lds16(b + 1024u + (uint32_t)(blk * 8 + 2 * l4));
-      raw.sb = sb_cur[r];
+      raw.sb = direct_sb ? __ldg(in.bsc[r] + gb) : __uint_as_float(lds32(b + 1152u + (uint32_t)(4 * blk)));
       float S[4];
       pay_scales<G, false>(raw, l4, S);
       if (r == 0) {
@@ -1030,8 +1028,6 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
     Quant q;
     quantize<G, false, false>(z, q);
     if (valid) store_block<G, false>(out, gb, l4, q);
-#pragma unroll
-    for (int r = 0; r < R; ++r) sb_cur[r] = sb_nxt[r];
   }
 }
 

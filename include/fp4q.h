@@ -127,7 +127,10 @@ fp4q_status fp4q_compress(const void* x_bf16, int64_t n, void* payload,
 /* Decompress-accumulate: payload (device) -> dst (device, n elements of dtype, 16-byte
  * aligned). dst = beta ? dst + x^ : x^, where x^ is the Decode step above; for a bfloat16
  * dst the sum is formed in FP32 and rounded to nearest even once. This is the receive side
- * of the compressed AllReduce [P3 "Read it as"]. dst may not overlap payload. */
+ * of the compressed AllReduce [P3 "Read it as"]. dst may not overlap payload. The payload
+ * is expected as fp4q_compress / fp4q_reduce_requantize write it (every block scale 0 or
+ * >= 2^-100); for other block scales the result can differ from the contract's decode in
+ * the last bit of values in the subnormal range. */
 fp4q_status fp4q_decompress_accumulate(const void* payload, int64_t n, void* dst,
                                        fp4q_dtype dtype, int32_t beta,
                                        const fp4q_params* params, void* stream);

@@ -254,3 +254,21 @@ def test_repeated_accumulate(dev):
         oracle.decompress_accumulate(pw, n, ref, beta=1)
     torch.cuda.synchronize()
     assert np.array_equal(d.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("G", [16, 32])
+@pytest.mark.parametrize("nb", [1, 2, 3, 4, 5, 6, 7, 9, 13, 8 * 97 + 3, 8 * 2431 + 7])
+def test_reduce_ragged_tails(dev, nb, G):
+    """Block counts with every remainder modulo the 8-block tile: the last tile's codes,
+    group scales and block scales are partly bulk-copied and partly loaded directly."""
+    n = 256 * nb
+    xs = [inputs.sweep(n, seed=s).ravel() for s in (5, 6, 7)]
+    for R in (1, 2, 3):
+        pays = [fq.compress(inputs.bits_to_torch(x, dev), group=G) for x in xs[:R]]
+        refs = [oracle.compress(x, group=G) for x in xs[:R]]
+        torch.cuda.synchronize()
+        for p, w in zip(pays, refs):
+            assert np.array_equal(p.cpu().numpy(), w)
+        red = fq.reduce_requantize(pays, n, group=G)
+        want, q = oracle.reduce_requantize(refs, n, G, want_q=True)
+        check_payload(red.cpu().numpy(), want, q, n, G, f"reduce nb={nb} R={R} G={G}")
