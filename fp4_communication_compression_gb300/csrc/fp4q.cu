@@ -46,11 +46,11 @@ constexpr int kTileBlocks = 8;                  // 256-element blocks per warp t
 // Warps per CTA and input stages per warp, per kernel (shared memory per warp decides how
 // many warps fit on an SM: compress and roundtrip are issue/latency bound and want the
 // most resident warps; one stage is enough because a tile's compute outlasts its load).
-constexpr int kCompressWarps = 3, kCompressStages = 1;
-constexpr int kRoundtripWarps = 3, kRoundtripStages = 1;
-constexpr int kDecompressWarps = 4, kDecompressStages = 1;
+constexpr int kCompressWarps = 4, kCompressStages = 1, kCompressCtas = 4;
+constexpr int kRoundtripWarps = 4, kRoundtripStages = 1, kRoundtripCtas = 4;
+constexpr int kDecompressWarps = 4, kDecompressStages = 1, kDecompressCtas = 4;
+constexpr int kDecompressGridCtas = 4;     // resident CTAs per SM the grid is sized for
 constexpr int kReduceWarps = 4;
-constexpr int kUnitsPerBlock = 73;              // 16-byte units per block in the transpose buffer
 constexpr float kZeroLimit = 2688.0f * 0x1p-100f;   // all-zero block guard on A_b
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -202,38 +202,68 @@ __device__ __forceinline__ void rows_bfly(Rows v, int hk) {
       for (int j = 0; j < 8; ++j) bfly2(v[k][j], v[k + hk][j]);
 }
 
-// Transpose buffer addressing: block region of 73 units, row r at unit
-// 4r + 2(r >> 2) + 2((r >> 1) & 1). Layout A rows 4a+k sit at 18a + 4k + 2(k >> 1);
-// layout B rows b+4k at 4b + 2(b >> 1) + 18k. Eight consecutive lanes (two blocks, four
-// rows each) then always touch eight distinct 16-byte bank groups.
-__device__ __forceinline__ int unitA(int blk, int a) { return kUnitsPerBlock * blk + 18 * a; }
-__device__ __forceinline__ int unitB(int blk, int b) { return kUnitsPerBlock * blk + 4 * b + 2 * (b >> 1); }
-__device__ __forceinline__ int offA(int k) { return 4 * k + 2 * (k >> 1); }
-__device__ __forceinline__ int offB(int k) { return 18 * k; }
+// Shared-memory vector accesses by 32-bit shared-window address.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Transpose buffer: block blk's 16 x 16 FP32 values fill 64 16-byte units (1 KiB, no
+// padding). Unit u = 4r + c (row r, 4-value chunk c) is stored at (u & ~7) | ((u & 7) ^ H)
+// with H = ((r >> 2) ^ (r & 3)) & 3 | (blk & 1) << 2. Then the 8 lanes of every access phase
+// (two blocks, four lanes each) hit 8 distinct 16-byte bank groups both when lanes own rows
+// 4a..4a+3 (layout A) and when they own rows b, b+4, b+8, b+12 (layout B), and the unit of
+// every access is a per-lane base (8 for layout A, 4 for layout B) plus an immediate.
+struct XposeAddr {
+  uint32_t a[8];   // layout A: unit base for (S ^ key), S = ((4 (j & 1) + c) ^ j) & 7
+  uint32_t b[4];   // layout B: unit base for ((c ^ k) & 3) ^ key
+};
+
+__device__ __forceinline__ XposeAddr xpose_addr(uint32_t xbuf, int blk, int l4) {
+  XposeAddr x;
+  const uint32_t blkb = xbuf + (uint32_t)blk * 1024u, beta4 = (uint32_t)(blk & 1) << 2;
+  const uint32_t keyA = (uint32_t)l4 | beta4;
+  const uint32_t keyB = ((4u * (uint32_t)(l4 & 1)) ^ (uint32_t)l4 ^ beta4) & 7u;
+  const uint32_t baseA = blkb + 256u * (uint32_t)l4, baseB = blkb + 128u * (uint32_t)(l4 >> 1);
+#pragma unroll
+  for (uint32_t s = 0; s < 8; ++s) x.a[s] = baseA + 16u * (s ^ keyA);
+#pragma unroll
+  for (uint32_t s = 0; s < 4; ++s) x.b[s] = baseB + 16u * (s ^ keyB);
+  return x;
+}
+// row 4 l4 + j, chunk c (layout A)
+__device__ __forceinline__ uint32_t xaddr_A(const XposeAddr& x, int j, int c) {
+  return x.a[((4 * (j & 1) + c) ^ j) & 7] + 128u * (uint32_t)(j >> 1);
+}
+// row l4 + 4k, chunk c (layout B)
+__device__ __forceinline__ uint32_t xaddr_B(const XposeAddr& x, int k, int c) {
+  return x.b[(c ^ k) & 3] + 256u * (uint32_t)k;
+}
 
 // Write the lane's 4 rows from one layout, read 4 rows of the other. toB: A -> B.
 template <bool toB>
-__device__ __forceinline__ void transpose(Rows v, float4* buf, int blk, int l4) {
-  const int wbase = toB ? unitA(blk, l4) : unitB(blk, l4);
-  const int rbase = toB ? unitB(blk, l4) : unitA(blk, l4);
+__device__ __forceinline__ void transpose(Rows v, const XposeAddr& x) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int o = toB ? offA(k) : offB(k);
+  for (int k = 0; k < 4; ++k)
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      buf[wbase + o + c] = make_float4(v[k][2 * c].x, v[k][2 * c].y, v[k][2 * c + 1].x, v[k][2 * c + 1].y);
-  }
+      sts128(toB ? xaddr_A(x, k, c) : xaddr_B(x, k, c),
+             make_uint4(__float_as_uint(v[k][2 * c].x), __float_as_uint(v[k][2 * c].y),
+                        __float_as_uint(v[k][2 * c + 1].x), __float_as_uint(v[k][2 * c + 1].y)));
   __syncwarp();
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int o = toB ? offB(k) : offA(k);
+  for (int k = 0; k < 4; ++k)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      float4 t = buf[rbase + o + c];
-      v[k][2 * c] = make_float2(t.x, t.y);
-      v[k][2 * c + 1] = make_float2(t.z, t.w);
+      const uint4 t = lds128(toB ? xaddr_B(x, k, c) : xaddr_A(x, k, c));
+      v[k][2 * c] = make_float2(__uint_as_float(t.x), __uint_as_float(t.y));
+      v[k][2 * c + 1] = make_float2(__uint_as_float(t.z), __uint_as_float(t.w));
     }
-  }
   __syncwarp();
 }
 
@@ -544,11 +574,6 @@ __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-  return v;
-}
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
@@ -558,10 +583,6 @@ __device__ __forceinline__ uint32_t lds16(uint32_t a) {
   uint16_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
   return v;
-}
-__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
 }
 
 // Device fault word: set when a bounded wait gives up (the kernel then drains its own copies
@@ -583,32 +604,30 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 
 constexpr int kTileLinesBF16 = 32;         // 128-byte lines per 8-block bf16 tile (4 KiB)
 constexpr int kTileLinesF32 = 64;          // 128-byte lines per 8-block f32 tile (8 KiB)
-constexpr int kXBufBytes = 10240;          // transpose buffer / output staging + barriers
-constexpr int kXBufUsed = kUnitsPerBlock * 16 * kTileBlocks;   // 9344 bytes of transpose data
+constexpr int kXBufBytes = 8192;           // transpose buffer / output staging per warp
+constexpr int kHeaderBytes = 1024;         // per-CTA header: every warp's stage barriers
 
-// Per-warp shared memory: [input stages][xbuf], every part 1024-byte aligned (the 128-byte
-// TMA swizzle repeats every 1024 bytes); the stage barriers sit in the xbuf's unused tail.
+// CTA shared memory: [alignment slack][header: 64 bytes of barriers per warp][warp regions],
+// each warp region = [input stages][xbuf], 1024-byte aligned (the 128-byte TMA swizzle
+// repeats every 1024 bytes).
 template <int WARPS, int STAGES, int IN_BYTES>
 struct WarpSmemLayout {
   static constexpr int kRegion = STAGES * IN_BYTES + kXBufBytes;
-  static constexpr int kCtaBytes = WARPS * kRegion + 1024;
+  static constexpr int kCtaBytes = 1024 + kHeaderBytes + WARPS * kRegion;
 };
 
 struct WarpSmem {
   uint32_t stage0, xbuf, bar0;
-  uint8_t* xbuf_ptr;
 };
 
 template <int STAGES, int IN_BYTES>
 __device__ __forceinline__ WarpSmem warp_smem(uint8_t* raw, int warp) {
   constexpr int region = STAGES * IN_BYTES + kXBufBytes;
-  const uint32_t raw_s = smem_addr(raw);
-  const uint32_t base = ((raw_s + 1023u) & ~1023u) + (uint32_t)(warp * region);
+  const uint32_t base = (smem_addr(raw) + 1023u) & ~1023u;
   WarpSmem w;
-  w.stage0 = base;
-  w.xbuf = base + STAGES * IN_BYTES;
-  w.bar0 = w.xbuf + kXBufUsed;
-  w.xbuf_ptr = raw + (w.xbuf - raw_s);
+  w.stage0 = base + kHeaderBytes + (uint32_t)(warp * region);
+  w.xbuf = w.stage0 + STAGES * IN_BYTES;
+  w.bar0 = base + 64u * (uint32_t)warp;
   return w;
 }
 
@@ -791,12 +810,12 @@ __device__ __forceinline__ void staging_store(const CUtensorMap* map, int lines,
 
 // K1: compress. x (bfloat16, n) -> payload. Input tiles arrive by TMA.
 template <int G, int FWHT>
-__global__ void __launch_bounds__(kCompressWarps * 32)
+__global__ void __launch_bounds__(kCompressWarps * 32, kCompressCtas)
 compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kCompressStages, 4096>(smem_raw, warp);
-  float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
+  const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
     mbar_expect_tx(bar, 4096);
     tma_load_2d(buf, &xmap, 0, (int32_t)(t * kTileLinesBF16), bar);
@@ -815,7 +834,7 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
       level1_fwd_from2(v);
       rows_bfly(v, 1);             // h = 16
       rows_bfly(v, 2);             // h = 32
-      transpose<true>(v, tbuf, blk, l4);
+      transpose<true>(v, xa);
       rows_bfly(v, 1);             // h = 64
       rows_bfly(v, 2);             // h = 128
       quantize<G, true, true>(v, q);
@@ -831,7 +850,7 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
 // The payload of the next tile is prefetched into registers; dst tiles are read (BETA) and
 // written through the swizzled shared staging buffer by TMA.
 template <int G, int FWHT, int DT, int BETA>
-__global__ void __launch_bounds__(kDecompressWarps * 32)
+__global__ void __launch_bounds__(kDecompressWarps * 32, kDecompressCtas)
 decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop T) {
   constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
   constexpr int LINES = DT == FP4Q_BF16 ? kTileLinesBF16 : kTileLinesF32;
@@ -839,7 +858,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kDecompressStages, BETA ? TB : 0>(smem_raw, warp);
-  float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
+  const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
     mbar_expect_tx(bar, TB);
     tma_load_2d(buf, &dmap, 0, (int32_t)(t * LINES), bar);
@@ -862,7 +881,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
     if (FWHT) {
       rows_bfly(v, 2);             // h = 128
       rows_bfly(v, 1);             // h = 64
-      transpose<false>(v, tbuf, blk, l4);
+      transpose<false>(v, xa);
       rows_bfly(v, 2);             // h = 32
       rows_bfly(v, 1);             // h = 16
       level1_inv(v);
@@ -892,12 +911,12 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
 
 // K3: fused roundtrip. x (bfloat16) -> y = bf16(decode(compress(x))), no payload.
 template <int G, int FWHT>
-__global__ void __launch_bounds__(kRoundtripWarps * 32)
+__global__ void __launch_bounds__(kRoundtripWarps * 32, kRoundtripCtas)
 roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap, TileLoop T) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kRoundtripStages, 4096>(smem_raw, warp);
-  float4* tbuf = reinterpret_cast<float4*>(ws.xbuf_ptr);
+  const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
     mbar_expect_tx(bar, 4096);
     tma_load_2d(buf, &xmap, 0, (int32_t)(t * kTileLinesBF16), bar);
@@ -916,7 +935,7 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       rows_bfly(v, 1);
       rows_bfly(v, 2);
       staging_free(lane);
-      transpose<true>(v, tbuf, blk, l4);
+      transpose<true>(v, xa);
       rows_bfly(v, 1);
       rows_bfly(v, 2);
       quantize<G, true, true>(v, q);
@@ -924,7 +943,7 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       dequantize(q.code, q.S, v, T.negzero);
       rows_bfly(v, 2);
       rows_bfly(v, 1);
-      transpose<false>(v, tbuf, blk, l4);
+      transpose<false>(v, xa);
       rows_bfly(v, 2);
       rows_bfly(v, 1);
       level1_inv(v);
@@ -1067,7 +1086,7 @@ struct Launch {
 
 // Persistent grid: as many CTAs as fit on all SMs at once, never more than the tiles need.
 template <typename K>
-fp4q_status plan(K kernel, int warps, int smem, int64_t tiles, Launch& L) {
+fp4q_status plan(K kernel, int warps, int smem, int64_t tiles, Launch& L, int max_per_sm = 0) {
   const int sms = num_sms();
   if (sms <= 0) return FP4Q_ERR_CUDA;
   if (smem > 48 * 1024 &&
@@ -1077,6 +1096,7 @@ fp4q_status plan(K kernel, int warps, int smem, int64_t tiles, Launch& L) {
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, warps * 32, smem) != cudaSuccess ||
       per_sm <= 0)
     return FP4Q_ERR_CUDA;
+  if (max_per_sm > 0 && per_sm > max_per_sm) per_sm = max_per_sm;
   const int64_t want = (tiles + warps - 1) / warps;
   const int64_t cap = (int64_t)per_sm * sms;
   L.grid = (int)(want < cap ? want : cap);
@@ -1168,7 +1188,8 @@ fp4q_status launch_decompress(const void* payload, int64_t n, void* dst, cudaStr
   constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
   Launch L;
   fp4q_status st = plan(k, kDecompressWarps,
-                        WarpSmemLayout<kDecompressWarps, kDecompressStages, B ? TB : 0>::kCtaBytes, T.tiles, L);
+                        WarpSmemLayout<kDecompressWarps, kDecompressStages, B ? TB : 0>::kCtaBytes, T.tiles, L,
+                        kDecompressGridCtas);
   if (st != FP4Q_OK) return st;
   k<<<L.grid, kDecompressWarps * 32, L.smem, s>>>(dm, payload_of(const_cast<void*>(payload), n, G), T);
   return launched();
