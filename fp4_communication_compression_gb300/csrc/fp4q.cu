@@ -50,7 +50,7 @@ constexpr int kCompressWarps = 4, kCompressStages = 1, kCompressCtas = 4;
 constexpr int kRoundtripWarps = 4, kRoundtripStages = 1, kRoundtripCtas = 4;
 constexpr int kDecompressWarps = 4, kDecompressStages = 1, kDecompressCtas = 4;
 constexpr int kDecompressGridCtas = 4;     // resident CTAs per SM the grid is sized for
-constexpr int kReduceWarps = 4;
+constexpr int kReduceWarps = 4, kReduceCtas = 4;
 constexpr float kZeroLimit = 2688.0f * 0x1p-100f;   // all-zero block guard on A_b
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -631,11 +631,12 @@ __device__ __forceinline__ WarpSmem warp_smem(uint8_t* raw, int warp) {
   return w;
 }
 
-// Per-warp input pipeline over STAGES stage buffers of BYTES bytes: lane 0 keeps STAGES
-// tiles in flight (issue(buf, bar, t) arms the barrier and starts the copies of tile t);
-// every lane waits on the tile's barrier, reads the stage, and the stage is refilled with
-// the tile STAGES iterations ahead.
-template <int STAGES, int BYTES>
+// Per-warp input pipeline over STAGES stage buffers of BYTES bytes: STAGES tiles stay in
+// flight (issue(buf, bar, t) arms the barrier and starts the copies of tile t; lane 0 calls
+// it, or every lane when ALL_LANES, for copies spread over lanes); every lane waits on the
+// tile's barrier, reads the stage, and the stage is refilled with the tile STAGES
+// iterations ahead.
+template <int STAGES, int BYTES, bool ALL_LANES = false>
 struct InPipe {
   uint32_t stage0, bar0;
   int64_t t0, W, tiles;
@@ -661,7 +662,7 @@ struct InPipe {
     for (int s = 0; s < STAGES; ++s) {
       const int64_t t = t0 + (int64_t)s * W;
       if (t < tiles) {
-        if (lane == 0) issue(buf(s), bar(s), t);
+        if (ALL_LANES || lane == 0) issue(buf(s), bar(s), t);
         ++issued;
       }
     }
@@ -691,7 +692,7 @@ struct InPipe {
     __syncwarp();
     const int64_t tn = t0 + (int64_t)(i + STAGES) * W;
     if (tn < tiles) {
-      if (lane == 0) issue(buf(i % STAGES), bar(i % STAGES), tn);
+      if (ALL_LANES || lane == 0) issue(buf(i % STAGES), bar(i % STAGES), tn);
       ++issued;
     }
     ++i;
@@ -987,28 +988,40 @@ struct ReduceCfg {
 };
 
 template <int G, int R>
-__global__ void __launch_bounds__(kReduceWarps * 32)
+__global__ void __launch_bounds__(kReduceWarps * 32, kReduceCtas)
 reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
   typedef ReduceCfg<R> C;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const uint32_t base = ((smem_addr(smem_raw) + 127u) & ~127u) + (uint32_t)(warp * C::kRegion);
   constexpr uint32_t gs_per_block = G == 16 ? 16 : 8;
+  // lane r < R copies rank r's segments; its three source pointers live in registers
+  const uint8_t* my_codes = in.codes[0];
+  const uint8_t* my_gsc = in.gsc[0];
+  const float* my_bsc = in.bsc[0];
+#pragma unroll
+  for (int r = 1; r < R; ++r)
+    if (lane == r) {
+      my_codes = in.codes[r];
+      my_gsc = in.gsc[r];
+      my_bsc = in.bsc[r];
+    }
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
     const int64_t left = T.nb - t * kTileBlocks;
     const uint32_t nblk = (uint32_t)(left < kTileBlocks ? left : kTileBlocks);
     const uint32_t cbytes = nblk * 128u, gbytes = (nblk * gs_per_block + 15u) & ~15u;
     const uint32_t sbytes = (nblk * 4u) & ~15u;
-    mbar_expect_tx(bar, (uint32_t)R * (cbytes + gbytes + sbytes));
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const uint32_t b = buf + (uint32_t)(r * kRankStageBytes);
-      bulk_load(b, in.codes[r] + t * 1024, cbytes, bar);
-      bulk_load(b + 1024, in.gsc[r] + t * (kTileBlocks * gs_per_block), gbytes, bar);
-      if (sbytes) bulk_load(b + 1152, in.bsc[r] + t * kTileBlocks, sbytes, bar);
+    // arm the barrier for all R ranks before any of their copies is issued
+    if (lane == 0) mbar_expect_tx(bar, (uint32_t)R * (cbytes + gbytes + sbytes));
+    __syncwarp();
+    if (lane < R) {
+      const uint32_t b = buf + (uint32_t)(lane * kRankStageBytes);
+      bulk_load(b, my_codes + t * 1024, cbytes, bar);
+      bulk_load(b + 1024, my_gsc + t * (kTileBlocks * gs_per_block), gbytes, bar);
+      if (sbytes) bulk_load(b + 1152, my_bsc + t * kTileBlocks, sbytes, bar);
     }
   };
-  InPipe<C::kStagesR, C::kStageBytes> pipe{};
+  InPipe<C::kStagesR, C::kStageBytes, true> pipe{};
   pipe.start(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), warp_global<kReduceWarps>(),
              warp_count<kReduceWarps>(), T.tiles, lane, issue);
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
