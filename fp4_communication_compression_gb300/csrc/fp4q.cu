@@ -37,6 +37,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <utility>
+
 #include "fp4q.h"
 #include "fp4q_math.cuh"
 
@@ -529,6 +531,14 @@ __device__ __forceinline__ void pay_scales(const PayRaw& r, int l4, float S[4]) 
 
 // ------------------------------------------------------------------ TMA pipelines
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation
+// may start while the previous kernel on the stream is finishing. griddepcontrol.wait blocks
+// until that kernel has completed and its memory operations are visible, so every kernel
+// calls it before its first global-memory access (read or write); launch_dependents lets the
+// next kernel's CTAs be scheduled as soon as SM resources free up.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Shared-memory primitives (sm_90+ PTX: mbarrier, cp.async.bulk.tensor, proxy fences).
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -814,6 +824,8 @@ template <int G, int FWHT>
 __global__ void __launch_bounds__(kCompressWarps * 32, kCompressCtas)
 compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T) {
   extern __shared__ uint8_t smem_raw[];
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kCompressStages, 4096>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
@@ -857,6 +869,8 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
   constexpr int LINES = DT == FP4Q_BF16 ? kTileLinesBF16 : kTileLinesF32;
   constexpr bool LB = FWHT != 0;
   extern __shared__ uint8_t smem_raw[];
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kDecompressStages, BETA ? TB : 0>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
@@ -915,6 +929,8 @@ template <int G, int FWHT>
 __global__ void __launch_bounds__(kRoundtripWarps * 32, kRoundtripCtas)
 roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap, TileLoop T) {
   extern __shared__ uint8_t smem_raw[];
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kRoundtripStages, 4096>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
@@ -992,6 +1008,8 @@ __global__ void __launch_bounds__(kReduceWarps * 32, kReduceCtas)
 reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
   typedef ReduceCfg<R> C;
   extern __shared__ uint8_t smem_raw[];
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const uint32_t base = ((smem_addr(smem_raw) + 127u) & ~127u) + (uint32_t)(warp * C::kRegion);
   constexpr uint32_t gs_per_block = G == 16 ? 16 : 8;
@@ -1117,6 +1135,22 @@ fp4q_status plan(K kernel, int warps, int smem, int64_t tiles, Launch& L, int ma
   return FP4Q_OK;
 }
 
+// Launch with programmatic stream serialisation (see grid_dependency_wait).
+template <class... KArgs, class... Args>
+fp4q_status launch_pdl(void (*kernel)(KArgs...), const Launch& L, int threads, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)L.grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = (size_t)L.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
 fp4q_status launched() { return cudaGetLastError() == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA; }
 
 // cuTensorMapEncodeTiled from the driver, looked up once.
@@ -1188,8 +1222,7 @@ fp4q_status launch_compress(const void* x, int64_t n, void* payload, cudaStream_
   fp4q_status st = plan(k, kCompressWarps, WarpSmemLayout<kCompressWarps, kCompressStages, 4096>::kCtaBytes,
                         T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kCompressWarps * 32, L.smem, s>>>(xm, payload_of(payload, n, G), T);
-  return launched();
+  return launch_pdl(k, L, kCompressWarps * 32, s, xm, payload_of(payload, n, G), T);
 }
 
 template <int G, int F, int DT, int B>
@@ -1204,8 +1237,7 @@ fp4q_status launch_decompress(const void* payload, int64_t n, void* dst, cudaStr
                         WarpSmemLayout<kDecompressWarps, kDecompressStages, B ? TB : 0>::kCtaBytes, T.tiles, L,
                         kDecompressGridCtas);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kDecompressWarps * 32, L.smem, s>>>(dm, payload_of(const_cast<void*>(payload), n, G), T);
-  return launched();
+  return launch_pdl(k, L, kDecompressWarps * 32, s, dm, payload_of(const_cast<void*>(payload), n, G), T);
 }
 
 template <int G, int F>
@@ -1218,8 +1250,7 @@ fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) 
   fp4q_status st = plan(k, kRoundtripWarps, WarpSmemLayout<kRoundtripWarps, kRoundtripStages, 4096>::kCtaBytes,
                         T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kRoundtripWarps * 32, L.smem, s>>>(xm, ym, T);
-  return launched();
+  return launch_pdl(k, L, kRoundtripWarps * 32, s, xm, ym, T);
 }
 
 template <int G, int R>
@@ -1229,8 +1260,7 @@ fp4q_status launch_reduce_r(const RankPtrs& in, int64_t n, void* out, cudaStream
   Launch L;
   fp4q_status st = plan(k, kReduceWarps, ReduceCfg<R>::kCtaBytes, T.tiles, L);
   if (st != FP4Q_OK) return st;
-  k<<<L.grid, kReduceWarps * 32, L.smem, s>>>(in, payload_of(out, n, G), T);
-  return launched();
+  return launch_pdl(k, L, kReduceWarps * 32, s, in, payload_of(out, n, G), T);
 }
 
 template <int G>

@@ -66,7 +66,10 @@
  * by fp4q_fault_flags). All entry points are asynchronous on the given
  * stream and never synchronise. Argument errors are returned before anything is launched.
  * A failed launch returns FP4Q_ERR_CUDA (the CUDA error is left to the caller's next
- * runtime call to report).
+ * runtime call to report). Kernels are launched with programmatic stream serialisation:
+ * a codec kernel may be scheduled while the previous kernel on the stream is finishing,
+ * but it waits for that kernel to complete (and for its memory to be visible) before its
+ * first global-memory access, so stream order is preserved exactly.
  */
 #ifndef FP4Q_H
 #define FP4Q_H

@@ -256,6 +256,36 @@ def test_repeated_accumulate(dev):
     assert np.array_equal(d.cpu().numpy(), ref)
 
 
+def test_back_to_back_chain_keeps_stream_order(dev):
+    """Kernels launched back to back with no host synchronisation, reusing buffers so that
+    each kernel writes what the previous one reads (the payloads) and reads what the previous
+    one wrote (the payloads and the accumulators): the kernels may start while their
+    predecessor finishes, so this checks that each waits for it before touching memory."""
+    n = 1 << 22
+    xs = [inputs.sweep(n, seed=s).ravel() for s in (11, 12, 13)]
+    xt = [inputs.bits_to_torch(x, dev) for x in xs]
+    p = [torch.empty(fq.payload_bytes(n), dtype=torch.uint8, device=dev) for _ in range(2)]
+    red = torch.empty_like(p[0])
+    d = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(xt[0])
+    torch.cuda.synchronize()
+    ref_d = np.zeros(n, np.uint16)
+    for it in range(4):
+        a, b = xs[it % 3], xs[(it + 1) % 3]
+        fq.compress(xt[it % 3], payload=p[0])
+        fq.compress(xt[(it + 1) % 3], payload=p[1])
+        fq.reduce_requantize(p, n, out=red)
+        fq.decompress_accumulate(red, n, d, beta=1)
+        fq.roundtrip(xt[it % 3], y=y)
+        ref_red = oracle.reduce_requantize([oracle.compress(a), oracle.compress(b)], n)
+        ref_d = oracle.decompress_accumulate(ref_red, n, ref_d, beta=1)
+    torch.cuda.synchronize()
+    assert np.array_equal(red.cpu().numpy(), ref_red)
+    assert np.array_equal(_bits(d), ref_d)
+    assert np.array_equal(_bits(y), oracle.roundtrip(xs[3 % 3]))
+    assert fq.fault_flags() == 0
+
+
 @pytest.mark.parametrize("G", [16, 32])
 @pytest.mark.parametrize("nb", [1, 2, 3, 4, 5, 6, 7, 9, 13, 8 * 97 + 3, 8 * 2431 + 7])
 def test_reduce_ragged_tails(dev, nb, G):
