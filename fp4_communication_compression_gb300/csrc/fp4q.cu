@@ -37,6 +37,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
 #include <utility>
 
 #include "fp4q.h"
@@ -1110,6 +1111,39 @@ int num_sms() {
   return g_num_sms[dev];
 }
 
+// Resident CTAs per SM of a kernel instance on the current device, with its dynamic
+// shared-memory limit raised as needed. Both runtime queries are made once per (kernel,
+// device) and cached: they cost microseconds of host time, which would otherwise be paid on
+// every call.
+struct PlanEntry {
+  const void* fn;
+  int dev, threads, smem, per_sm;
+};
+std::mutex g_plan_mu;
+PlanEntry g_plan[512];
+int g_plan_count = 0;
+
+int resident_ctas(const void* fn, int threads, int smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    for (int i = 0; i < g_plan_count; ++i) {
+      const PlanEntry& e = g_plan[i];
+      if (e.fn == fn && e.dev == dev && e.threads == threads && e.smem == smem) return e.per_sm;
+    }
+  }
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -1;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess || per_sm <= 0)
+    return -1;
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  if (g_plan_count < (int)(sizeof(g_plan) / sizeof(g_plan[0]))) g_plan[g_plan_count++] = {fn, dev, threads, smem, per_sm};
+  return per_sm;
+}
+
 struct Launch {
   int grid;
   int smem;
@@ -1120,13 +1154,8 @@ template <typename K>
 fp4q_status plan(K kernel, int warps, int smem, int64_t tiles, Launch& L, int max_per_sm = 0) {
   const int sms = num_sms();
   if (sms <= 0) return FP4Q_ERR_CUDA;
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return FP4Q_ERR_CUDA;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, warps * 32, smem) != cudaSuccess ||
-      per_sm <= 0)
-    return FP4Q_ERR_CUDA;
+  int per_sm = resident_ctas(reinterpret_cast<const void*>(kernel), warps * 32, smem);
+  if (per_sm <= 0) return FP4Q_ERR_CUDA;
   if (max_per_sm > 0 && per_sm > max_per_sm) per_sm = max_per_sm;
   const int64_t want = (tiles + warps - 1) / warps;
   const int64_t cap = (int64_t)per_sm * sms;
