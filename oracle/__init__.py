@@ -53,15 +53,18 @@ def _load():
             "oracle_e2m1_decode": (ctypes.c_float, [ctypes.c_uint8]),
             "oracle_e2m1_encode": (ctypes.c_uint8, [ctypes.c_float]),
             "oracle_fwht256": (None, [P]),
-            "oracle_payload_bytes": (I64, [I64, I]),
-            "oracle_gscale_offset": (I64, [I64, I]),
-            "oracle_bscale_offset": (I64, [I64, I]),
+            "oracle_payload_bytes": (I64, [I64, I, I]),
+            "oracle_gscale_offset": (I64, [I64, I, I]),
+            "oracle_bscale_offset": (I64, [I64, I, I]),
+            "oracle_e8m0_scale": (ctypes.c_uint8, [ctypes.c_float]),
+            "oracle_e8m0_decode": (ctypes.c_float, [ctypes.c_uint8]),
+            "oracle_e8m0_scale_array": (None, [P, P, I64]),
             "oracle_max_threads": (I, []),
             "oracle_set_threads": (None, [I]),
-            "oracle_compress": (I, [P, I64, P, I, I, P]),
-            "oracle_decompress_accumulate": (I, [P, I64, P, I, I, I, I]),
-            "oracle_roundtrip": (I, [P, I64, P, I, I]),
-            "oracle_reduce_requantize": (I, [P, I, I64, P, I, P]),
+            "oracle_compress": (I, [P, I64, P, I, I, I, P]),
+            "oracle_decompress_accumulate": (I, [P, I64, P, I, I, I, I, I]),
+            "oracle_roundtrip": (I, [P, I64, P, I, I, I]),
+            "oracle_reduce_requantize": (I, [P, I, I64, P, I, I, P]),
             "oracle_e4m3_encode_array": (None, [P, P, I64]),
             "oracle_e2m1_encode_array": (None, [P, P, I64]),
             "oracle_bf16_round_array": (None, [P, P, I64]),
@@ -141,37 +144,68 @@ def fwht256(v, inverse: bool = False) -> np.ndarray:
 
 
 # ------------------------------------------------------------------ codec
+#
+# scales = "dual": E4M3 group scale x FP32 block scale (group 16 or 32, default 16);
+# scales = "e8m0": microscaled variant, power-of-two E8M0 scale per group of 32 and no block
+# scale (group 32, the default for it).
 
-def payload_bytes(n: int, group: int = 16) -> int:
-    return int(_load().oracle_payload_bytes(int(n), int(group)))
-
-
-def gscale_offset(n: int, group: int = 16) -> int:
-    return int(_load().oracle_gscale_offset(int(n), int(group)))
-
-
-def bscale_offset(n: int, group: int = 16) -> int:
-    return int(_load().oracle_bscale_offset(int(n), int(group)))
+SCALES = {"dual": 0, "e8m0": 1}
 
 
-def compress(x_bf16: np.ndarray, group: int = 16, fwht: int = 1, want_q: bool = False):
+def _fmt(group, scales):
+    if scales not in SCALES:
+        raise ValueError(f"scales must be one of {sorted(SCALES)}")
+    mx = SCALES[scales]
+    return (int(group) if group is not None else (32 if mx else 16)), mx
+
+
+def e8m0_scale(amax) -> np.ndarray:
+    a = np.ascontiguousarray(amax, dtype=np.float32).ravel()
+    out = np.empty(a.size, np.uint8)
+    _load().oracle_e8m0_scale_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    return np.array([_load().oracle_e8m0_decode(int(c)) for c in np.ravel(codes)], np.float32)
+
+
+def payload_bytes(n: int, group: int | None = None, scales: str = "dual") -> int:
+    G, mx = _fmt(group, scales)
+    return int(_load().oracle_payload_bytes(int(n), G, mx))
+
+
+def gscale_offset(n: int, group: int | None = None, scales: str = "dual") -> int:
+    G, mx = _fmt(group, scales)
+    return int(_load().oracle_gscale_offset(int(n), G, mx))
+
+
+def bscale_offset(n: int, group: int | None = None, scales: str = "dual") -> int:
+    G, mx = _fmt(group, scales)
+    return int(_load().oracle_bscale_offset(int(n), G, mx))
+
+
+def compress(x_bf16: np.ndarray, group: int | None = None, fwht: int = 1, want_q: bool = False,
+             scales: str = "dual"):
     """x_bf16: uint16 bit patterns. Returns the payload (uint8) and, if want_q, every q."""
+    G, mx = _fmt(group, scales)
     x = _c(x_bf16, np.uint16).ravel()
     n = x.size
-    nbytes = payload_bytes(n, group)
+    nbytes = payload_bytes(n, G, scales)
     if nbytes == 0:
-        raise ValueError(f"invalid n={n} or group={group}")
+        raise ValueError(f"invalid n={n} or group={G} for scales={scales}")
     out = np.zeros(nbytes, np.uint8)
     q = np.empty(n, np.float32) if want_q else None
-    rc = _load().oracle_compress(_ptr(x), n, _ptr(out), group, fwht, _ptr(q) if want_q else None)
+    rc = _load().oracle_compress(_ptr(x), n, _ptr(out), G, fwht, mx, _ptr(q) if want_q else None)
     if rc != 0:
         raise ValueError(f"oracle_compress failed ({rc})")
     return (out, q) if want_q else out
 
 
 def decompress_accumulate(payload: np.ndarray, n: int, dst: np.ndarray, beta: int,
-                          group: int = 16, fwht: int = 1) -> np.ndarray:
+                          group: int | None = None, fwht: int = 1, scales: str = "dual") -> np.ndarray:
     """dst: uint16 (bfloat16 bits) or float32 array of n elements, updated in place."""
+    G, mx = _fmt(group, scales)
     p = _c(payload, np.uint8)
     if dst.dtype == np.uint16:
         dtype = 0
@@ -181,38 +215,44 @@ def decompress_accumulate(payload: np.ndarray, n: int, dst: np.ndarray, beta: in
         raise TypeError("dst must be uint16 (bfloat16 bits) or float32")
     assert dst.flags.c_contiguous and dst.size == n
     rc = _load().oracle_decompress_accumulate(_ptr(p), int(n), _ptr(dst), dtype, int(beta),
-                                              group, fwht)
+                                              G, fwht, mx)
     if rc != 0:
         raise ValueError(f"oracle_decompress_accumulate failed ({rc})")
     return dst
 
 
-def roundtrip(x_bf16: np.ndarray, group: int = 16, fwht: int = 1) -> np.ndarray:
+def roundtrip(x_bf16: np.ndarray, group: int | None = None, fwht: int = 1,
+              scales: str = "dual") -> np.ndarray:
+    G, mx = _fmt(group, scales)
     x = _c(x_bf16, np.uint16).ravel()
     y = np.empty_like(x)
-    rc = _load().oracle_roundtrip(_ptr(x), x.size, _ptr(y), group, fwht)
+    rc = _load().oracle_roundtrip(_ptr(x), x.size, _ptr(y), G, fwht, mx)
     if rc != 0:
         raise ValueError(f"oracle_roundtrip failed ({rc})")
     return y
 
 
-def reduce_requantize(payloads, n: int, group: int = 16, want_q: bool = False):
+def reduce_requantize(payloads, n: int, group: int | None = None, want_q: bool = False,
+                      scales: str = "dual"):
+    G, mx = _fmt(group, scales)
     ps = [_c(p, np.uint8) for p in payloads]
     R = len(ps)
     arr = (ctypes.c_void_p * R)(*[_ptr(p) for p in ps])
-    out = np.zeros(payload_bytes(n, group), np.uint8)
+    out = np.zeros(payload_bytes(n, G, scales), np.uint8)
     q = np.empty(n, np.float32) if want_q else None
     rc = _load().oracle_reduce_requantize(ctypes.cast(arr, ctypes.c_void_p), R, int(n), _ptr(out),
-                                          group, _ptr(q) if want_q else None)
+                                          G, mx, _ptr(q) if want_q else None)
     if rc != 0:
         raise ValueError(f"oracle_reduce_requantize failed ({rc})")
     return (out, q) if want_q else out
 
 
-def split_payload(payload: np.ndarray, n: int, group: int = 16):
-    """(codes uint8[n/2], gscale uint8[n/G], bscale float32[n/256]) views of a payload."""
-    g0, b0 = gscale_offset(n, group), bscale_offset(n, group)
+def split_payload(payload: np.ndarray, n: int, group: int | None = None, scales: str = "dual"):
+    """(codes uint8[n/2], gscale uint8[n/G], bscale float32[n/256]) views of a payload (the
+    block scales are empty for scales="e8m0")."""
+    G, mx = _fmt(group, scales)
+    g0, b0 = gscale_offset(n, G, scales), bscale_offset(n, G, scales)
     codes = payload[:n // 2]
-    gsc = payload[g0:g0 + n // group]
-    bsc = payload[b0:b0 + 4 * (n // BLOCK)].view(np.float32)
+    gsc = payload[g0:g0 + n // G]
+    bsc = payload[b0:b0 + (0 if mx else 4 * (n // BLOCK))].view(np.float32)
     return codes, gsc, bsc

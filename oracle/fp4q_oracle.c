@@ -16,7 +16,8 @@
  *        factors", "packed two per byte", "a fast transform keeps errors low") and
  *        "Read it as" (the AllReduce of tensor parallelism is what is compressed).
  *   [P4] "Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs"
- *        (gist.science), technical summary, problem statement: FP4 elements are E2M1.
+ *        (gist.science), technical summary, problem statement: FP4 elements are E2M1, and
+ *        the microscaled MXFP4 format scales blocks of 32 elements.
  * The pages give no numbers. The numbers used here (block 256, FWHT as 16 x 16 in Sylvester
  * order, group 16 or 32, E4M3 group scale x FP32 block scale with 2688 = 6 * 448, ties to
  * even, the -0 code, the all-zero guard, the payload layout) are the build's stated
@@ -117,6 +118,26 @@ uint8_t oracle_e2m1_encode(float q) {
   return (uint8_t)(sign | best);
 }
 
+/* ---------------------------------------------------------------- E8M0 (MX scale) */
+
+/* The microscaled variant [P4 problem statement: MXFP4 scales blocks of 32 E2M1 elements]
+ * gives each group of 32 a power-of-two scale X stored as an 8-bit exponent (E8M0: code =
+ * exponent + 127). The reading follows the open MX definition: X = 2^(floor(log2(amax)) -
+ * 2), where 2 is the exponent of the largest E2M1 value (6 = 1.5 * 2^2), so amax / X lies
+ * in [4, 8); the exponent is clamped below at -127 (code 0, which also serves amax = 0).
+ * floor(log2(a)) comes from frexpf (a = m * 2^e with m in [0.5, 1)), exact for subnormals. */
+uint8_t oracle_e8m0_scale(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int e = 0;
+  frexpf(amax, &e);
+  int shared = (e - 1) - 2;
+  if (shared < -127) shared = -127;
+  return (uint8_t)(shared + 127);
+}
+
+/* Value of an E8M0 scale code: 2^(code - 127) (code 255 is NaN and never produced). */
+float oracle_e8m0_decode(uint8_t code) { return ldexpf(1.0f, (int)code - 127); }
+
 /* ---------------------------------------------------------------- FWHT */
 
 /* Orthonormal Walsh-Hadamard transform of one 256-element block in Sylvester (natural)
@@ -157,19 +178,25 @@ void oracle_ifwht256(float* v) {
 
 static int64_t pad16(int64_t b) { return (b + 15) / 16 * 16; }
 
-static int valid(int64_t n, int G) {
-  return n > 0 && n % ORACLE_BLOCK == 0 && n < ((int64_t)1 << 40) && (G == 16 || G == 32);
+/* mx = 0: dual scales (E4M3 per group x FP32 per block), G = 16 or 32;
+ * mx = 1: E8M0 power-of-two scale per group of 32, no block scale. */
+static int valid(int64_t n, int G, int mx) {
+  if (mx != 0 && mx != 1) return 0;
+  if (mx ? G != 32 : (G != 16 && G != 32)) return 0;
+  return n > 0 && n % ORACLE_BLOCK == 0 && n < ((int64_t)1 << 40);
 }
 
 /* Payload = [codes n/2 bytes][group scales n/G bytes, padded to 16][block scales n/256
- * float32]. [P3 "values are packed two per byte"; the layout itself is the build's
- * reading, the pages give none] Returns 0 on invalid arguments. */
-int64_t oracle_payload_bytes(int64_t n, int G) {
-  if (!valid(n, G)) return 0;
-  return n / 2 + pad16(n / G) + 4 * (n / ORACLE_BLOCK);
+ * float32; absent when mx]. [P3 "values are packed two per byte"; the layout itself is the
+ * build's reading, the pages give none] Returns 0 on invalid arguments. */
+int64_t oracle_payload_bytes(int64_t n, int G, int mx) {
+  if (!valid(n, G, mx)) return 0;
+  return n / 2 + pad16(n / G) + (mx ? 0 : 4 * (n / ORACLE_BLOCK));
 }
-int64_t oracle_gscale_offset(int64_t n, int G) { return valid(n, G) ? n / 2 : 0; }
-int64_t oracle_bscale_offset(int64_t n, int G) { return valid(n, G) ? n / 2 + pad16(n / G) : 0; }
+int64_t oracle_gscale_offset(int64_t n, int G, int mx) { return valid(n, G, mx) ? n / 2 : 0; }
+int64_t oracle_bscale_offset(int64_t n, int G, int mx) {
+  return valid(n, G, mx) ? n / 2 + pad16(n / G) : 0;
+}
 
 /* ---------------------------------------------------------------- one block */
 
@@ -229,6 +256,37 @@ static void dequantize_block(const uint8_t* packed, const uint8_t* gs, float s_b
   }
 }
 
+/* Microscaled quantisation of one block (8 groups of 32): per group X = E8M0 scale of
+ * amax, q = y / X (a division by a power of two), code = E2M1(q). No block-level guard:
+ * a group of zeros gets scale code 0 and codes 0x0 / 0x8 by the sign of each zero. */
+static void quantize_block_mx(const float* y, uint8_t* code, uint8_t* gs, float* q_out) {
+  for (int g = 0; g < ORACLE_BLOCK / 32; ++g) {
+    const float* yg = y + g * 32;
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+      float a = fabsf(yg[i]);
+      if (a > amax) amax = a;
+    }
+    uint8_t sc = oracle_e8m0_scale(amax);
+    gs[g] = sc;
+    float X = oracle_e8m0_decode(sc);
+    for (int i = 0; i < 32; ++i) {
+      float q = yg[i] / X;
+      code[g * 32 + i] = oracle_e2m1_encode(q);
+      if (q_out) q_out[g * 32 + i] = q;
+    }
+  }
+}
+
+/* Decoded transform-domain values of a microscaled block: x~ = grid(code) * X. */
+static void dequantize_block_mx(const uint8_t* packed, const uint8_t* gs, float* out) {
+  for (int i = 0; i < ORACLE_BLOCK; ++i) {
+    uint8_t byte = packed[i / 2];
+    uint8_t c = (i % 2 == 0) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);
+    out[i] = oracle_e2m1_decode(c) * oracle_e8m0_decode(gs[i / 32]);
+  }
+}
+
 /* Two codes per byte, the even element in the low nibble [P3 "packed two per byte"]. */
 static void pack_block(const uint8_t* code, uint8_t* packed) {
   for (int k = 0; k < ORACLE_BLOCK / 2; ++k)
@@ -256,13 +314,13 @@ void oracle_set_threads(int t) {
 /* Compress: per block, widen BF16 to FP32, FWHT (if fwht), quantise, pack.
  * Returns 0, or -1 on invalid arguments. q_out (optional) receives the pre-rounding q of
  * every element. */
-int oracle_compress(const uint16_t* x, int64_t n, uint8_t* payload, int G, int fwht,
+int oracle_compress(const uint16_t* x, int64_t n, uint8_t* payload, int G, int fwht, int mx,
                     float* q_out) {
-  if (!valid(n, G) || (fwht != 0 && fwht != 1) || !x || !payload) return -1;
+  if (!valid(n, G, mx) || (fwht != 0 && fwht != 1) || !x || !payload) return -1;
   int64_t nb = n / ORACLE_BLOCK;
   uint8_t* codes = payload;
-  uint8_t* gsc = payload + oracle_gscale_offset(n, G);
-  float* bsc = (float*)(payload + oracle_bscale_offset(n, G));
+  uint8_t* gsc = payload + oracle_gscale_offset(n, G, mx);
+  float* bsc = (float*)(payload + oracle_bscale_offset(n, G, mx));
   memset(gsc + n / G, 0, (size_t)(pad16(n / G) - n / G));
 #pragma omp parallel for schedule(static)
   for (int64_t b = 0; b < nb; ++b) {
@@ -271,9 +329,13 @@ int oracle_compress(const uint16_t* x, int64_t n, uint8_t* payload, int G, int f
     float s_b;
     for (int i = 0; i < ORACLE_BLOCK; ++i) y[i] = oracle_bf16_to_f32(x[b * ORACLE_BLOCK + i]);
     if (fwht) oracle_fwht256(y);
-    quantize_block(y, G, code, gsc + b * (ORACLE_BLOCK / G), &s_b,
-                   q_out ? q_out + b * ORACLE_BLOCK : NULL);
-    memcpy(&bsc[b], &s_b, 4);
+    if (mx) {
+      quantize_block_mx(y, code, gsc + b * (ORACLE_BLOCK / 32), q_out ? q_out + b * ORACLE_BLOCK : NULL);
+    } else {
+      quantize_block(y, G, code, gsc + b * (ORACLE_BLOCK / G), &s_b,
+                     q_out ? q_out + b * ORACLE_BLOCK : NULL);
+      memcpy(&bsc[b], &s_b, 4);
+    }
     pack_block(code, codes + b * (ORACLE_BLOCK / 2));
   }
   return 0;
@@ -281,14 +343,18 @@ int oracle_compress(const uint16_t* x, int64_t n, uint8_t* payload, int G, int f
 
 /* Decode block b of a payload to 256 FP32 values: x~ = grid(code) * S, then the inverse
  * FWHT (mirror stage order) when fwht is set. */
-static void decode_all(const uint8_t* payload, int64_t n, int G, int fwht, int64_t b,
+static void decode_all(const uint8_t* payload, int64_t n, int G, int fwht, int mx, int64_t b,
                        float* xh) {
   const uint8_t* codes = payload;
-  const uint8_t* gsc = payload + oracle_gscale_offset(n, G);
-  const uint8_t* bsc = payload + oracle_bscale_offset(n, G);
-  float s_b;
-  memcpy(&s_b, bsc + 4 * b, 4);
-  dequantize_block(codes + b * (ORACLE_BLOCK / 2), gsc + b * (ORACLE_BLOCK / G), s_b, G, xh);
+  const uint8_t* gsc = payload + oracle_gscale_offset(n, G, mx);
+  if (mx) {
+    dequantize_block_mx(codes + b * (ORACLE_BLOCK / 2), gsc + b * (ORACLE_BLOCK / 32), xh);
+  } else {
+    const uint8_t* bsc = payload + oracle_bscale_offset(n, G, mx);
+    float s_b;
+    memcpy(&s_b, bsc + 4 * b, 4);
+    dequantize_block(codes + b * (ORACLE_BLOCK / 2), gsc + b * (ORACLE_BLOCK / G), s_b, G, xh);
+  }
   if (fwht) oracle_ifwht256(xh);
 }
 
@@ -296,15 +362,15 @@ static void decode_all(const uint8_t* payload, int64_t n, int G, int fwht, int64
  * in FP32 and rounded once to nearest even; dtype 1: float32 dst). The receive side of the
  * compressed AllReduce [P3 "Read it as"]. Returns 0, or -1 on invalid arguments. */
 int oracle_decompress_accumulate(const uint8_t* payload, int64_t n, void* dst, int dtype,
-                                 int beta, int G, int fwht) {
-  if (!valid(n, G) || (fwht != 0 && fwht != 1) || (dtype != 0 && dtype != 1) ||
+                                 int beta, int G, int fwht, int mx) {
+  if (!valid(n, G, mx) || (fwht != 0 && fwht != 1) || (dtype != 0 && dtype != 1) ||
       (beta != 0 && beta != 1) || !payload || !dst)
     return -1;
   int64_t nb = n / ORACLE_BLOCK;
 #pragma omp parallel for schedule(static)
   for (int64_t b = 0; b < nb; ++b) {
     float xh[ORACLE_BLOCK];
-    decode_all(payload, n, G, fwht, b, xh);
+    decode_all(payload, n, G, fwht, mx, b, xh);
     for (int i = 0; i < ORACLE_BLOCK; ++i) {
       int64_t e = b * ORACLE_BLOCK + i;
       if (dtype == 0) {
@@ -321,13 +387,13 @@ int oracle_decompress_accumulate(const uint8_t* payload, int64_t n, void* dst, i
 }
 
 /* Roundtrip: y = bf16(decode(compress(x))), the definition of the fused fake-quantizer. */
-int oracle_roundtrip(const uint16_t* x, int64_t n, uint16_t* y, int G, int fwht) {
-  int64_t bytes = oracle_payload_bytes(n, G);
+int oracle_roundtrip(const uint16_t* x, int64_t n, uint16_t* y, int G, int fwht, int mx) {
+  int64_t bytes = oracle_payload_bytes(n, G, mx);
   if (bytes == 0 || !x || !y) return -1;
   uint8_t* p = (uint8_t*)malloc((size_t)bytes);
   if (!p) return -2;
-  int rc = oracle_compress(x, n, p, G, fwht, NULL);
-  if (rc == 0) rc = oracle_decompress_accumulate(p, n, y, 0, 0, G, fwht);
+  int rc = oracle_compress(x, n, p, G, fwht, mx, NULL);
+  if (rc == 0) rc = oracle_decompress_accumulate(p, n, y, 0, 0, G, fwht, mx);
   free(p);
   return rc;
 }
@@ -337,28 +403,32 @@ int oracle_roundtrip(const uint16_t* x, int64_t n, uint16_t* y, int G, int fwht)
  * packed again with no forward FWHT. [P3 "Read it as": the tensor-parallel AllReduce]
  * Returns 0, or -1 on invalid arguments. */
 int oracle_reduce_requantize(const uint8_t* const* payloads, int R, int64_t n, uint8_t* out,
-                             int G, float* q_out) {
-  if (!valid(n, G) || R < 1 || R > ORACLE_MAX_RANKS || !payloads || !out) return -1;
+                             int G, int mx, float* q_out) {
+  if (!valid(n, G, mx) || R < 1 || R > ORACLE_MAX_RANKS || !payloads || !out) return -1;
   for (int r = 0; r < R; ++r)
     if (!payloads[r]) return -1;
   int64_t nb = n / ORACLE_BLOCK;
   uint8_t* codes = out;
-  uint8_t* gsc = out + oracle_gscale_offset(n, G);
-  float* bsc = (float*)(out + oracle_bscale_offset(n, G));
+  uint8_t* gsc = out + oracle_gscale_offset(n, G, mx);
+  float* bsc = (float*)(out + oracle_bscale_offset(n, G, mx));
   memset(gsc + n / G, 0, (size_t)(pad16(n / G) - n / G));
 #pragma omp parallel for schedule(static)
   for (int64_t b = 0; b < nb; ++b) {
     float z[ORACLE_BLOCK], xr[ORACLE_BLOCK];
     uint8_t code[ORACLE_BLOCK];
     float s_b;
-    decode_all(payloads[0], n, G, 0, b, z);
+    decode_all(payloads[0], n, G, 0, mx, b, z);
     for (int r = 1; r < R; ++r) {
-      decode_all(payloads[r], n, G, 0, b, xr);
+      decode_all(payloads[r], n, G, 0, mx, b, xr);
       for (int i = 0; i < ORACLE_BLOCK; ++i) z[i] = z[i] + xr[i];
     }
-    quantize_block(z, G, code, gsc + b * (ORACLE_BLOCK / G), &s_b,
-                   q_out ? q_out + b * ORACLE_BLOCK : NULL);
-    memcpy(&bsc[b], &s_b, 4);
+    if (mx) {
+      quantize_block_mx(z, code, gsc + b * (ORACLE_BLOCK / 32), q_out ? q_out + b * ORACLE_BLOCK : NULL);
+    } else {
+      quantize_block(z, G, code, gsc + b * (ORACLE_BLOCK / G), &s_b,
+                     q_out ? q_out + b * ORACLE_BLOCK : NULL);
+      memcpy(&bsc[b], &s_b, 4);
+    }
     pack_block(code, codes + b * (ORACLE_BLOCK / 2));
   }
   return 0;
@@ -374,6 +444,11 @@ void oracle_e4m3_encode_array(const float* r, uint8_t* out, int64_t n) {
 void oracle_e2m1_encode_array(const float* q, uint8_t* out, int64_t n) {
 #pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_encode(q[i]);
+}
+
+void oracle_e8m0_scale_array(const float* a, uint8_t* out, int64_t n) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e8m0_scale(a[i]);
 }
 
 void oracle_bf16_round_array(const float* f, uint16_t* out, int64_t n) {
