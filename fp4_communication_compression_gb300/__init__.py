@@ -9,6 +9,11 @@ and returns without synchronising. The codec itself runs only in the sm_103a ker
     decompress_accumulate(payload, x.numel(), dst, beta=1) # dst += decode(payload)
     y = roundtrip(x)                                       # fused fake-quantisation
     out = reduce_requantize([p0, p1, p2, p3], n)           # emulated 4-rank reduce
+    p = compress(x, scales="e8m0")                         # microscaled variant (group 32)
+
+``scales="dual"`` (default) is the E4M3 group scale x FP32 block scale format (group 16 or
+32); ``scales="e8m0"`` the power-of-two scale per group of 32 with no block scale. Every
+call on one payload must use the same group, fwht and scales.
 
 Method: "FP4Quant: Efficient 4-Bit Communication Compression for Model-Parallel LLM
 Training" (abstract: micro-grouped dual-scale FP4 quantization, warp-cooperative FP4
@@ -45,41 +50,41 @@ def _dev(t, name):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def payload_bytes(n: int, group: int = 16, fwht: int = 1) -> int:
-    p = _lib.params(group, fwht)
+def payload_bytes(n: int, group: int | None = None, fwht: int = 1, scales: str = "dual") -> int:
+    p = _lib.params(group, fwht, scales=scales)
     return int(_lib.lib().fp4q_payload_bytes(int(n), ctypes.byref(p)))
 
 
-def gscale_offset(n: int, group: int = 16, fwht: int = 1) -> int:
-    p = _lib.params(group, fwht)
+def gscale_offset(n: int, group: int | None = None, fwht: int = 1, scales: str = "dual") -> int:
+    p = _lib.params(group, fwht, scales=scales)
     return int(_lib.lib().fp4q_gscale_offset(int(n), ctypes.byref(p)))
 
 
-def bscale_offset(n: int, group: int = 16, fwht: int = 1) -> int:
-    p = _lib.params(group, fwht)
+def bscale_offset(n: int, group: int | None = None, fwht: int = 1, scales: str = "dual") -> int:
+    p = _lib.params(group, fwht, scales=scales)
     return int(_lib.lib().fp4q_bscale_offset(int(n), ctypes.byref(p)))
 
 
-def compress(x, payload=None, group: int = 16, fwht: int = 1, stream=None):
+def compress(x, payload=None, group: int | None = None, fwht: int = 1, stream=None, scales: str = "dual"):
     """bfloat16 CUDA tensor -> uint8 payload tensor (allocated by torch if not given)."""
     import torch
     if x.dtype != torch.bfloat16:
         raise TypeError("x must be bfloat16")
     n = x.numel()
     if payload is None:
-        nb = payload_bytes(n, group, fwht)
+        nb = payload_bytes(n, group, fwht, scales)
         if nb == 0:
             raise ValueError(f"invalid size {n} (must be a positive multiple of 256)")
         payload = torch.empty(nb, dtype=torch.uint8, device=x.device)
-    p = _lib.params(group, fwht)
+    p = _lib.params(group, fwht, scales=scales)
     st = _lib.lib().fp4q_compress(_dev(x, "x"), n, _dev(payload, "payload"), ctypes.byref(p),
                                   _stream(stream, x.device))
     _lib.check("fp4q_compress", st)
     return payload
 
 
-def decompress_accumulate(payload, n: int, dst, beta: int = 1, group: int = 16, fwht: int = 1,
-                          stream=None):
+def decompress_accumulate(payload, n: int, dst, beta: int = 1, group: int | None = None, fwht: int = 1,
+                          stream=None, scales: str = "dual"):
     """dst (bfloat16 or float32 CUDA tensor of n elements) = beta ? dst + x^ : x^."""
     import torch
     if dst.dtype == torch.bfloat16:
@@ -90,7 +95,7 @@ def decompress_accumulate(payload, n: int, dst, beta: int = 1, group: int = 16, 
         raise TypeError("dst must be bfloat16 or float32")
     if dst.numel() != n:
         raise ValueError("dst must have n elements")
-    p = _lib.params(group, fwht)
+    p = _lib.params(group, fwht, scales=scales)
     st = _lib.lib().fp4q_decompress_accumulate(_dev(payload, "payload"), int(n), _dev(dst, "dst"),
                                                dt, int(beta), ctypes.byref(p),
                                                _stream(stream, dst.device))
@@ -98,29 +103,30 @@ def decompress_accumulate(payload, n: int, dst, beta: int = 1, group: int = 16, 
     return dst
 
 
-def roundtrip(x, y=None, group: int = 16, fwht: int = 1, stream=None):
+def roundtrip(x, y=None, group: int | None = None, fwht: int = 1, stream=None, scales: str = "dual"):
     """y = bf16(decode(compress(x))) in one kernel, no payload written."""
     import torch
     if x.dtype != torch.bfloat16:
         raise TypeError("x must be bfloat16")
     if y is None:
         y = torch.empty_like(x)
-    p = _lib.params(group, fwht)
+    p = _lib.params(group, fwht, scales=scales)
     st = _lib.lib().fp4q_roundtrip(_dev(x, "x"), x.numel(), _dev(y, "y"), ctypes.byref(p),
                                    _stream(stream, x.device))
     _lib.check("fp4q_roundtrip", st)
     return y
 
 
-def reduce_requantize(payloads, n: int, out=None, group: int = 16, fwht: int = 1, stream=None):
+def reduce_requantize(payloads, n: int, out=None, group: int | None = None, fwht: int = 1, stream=None,
+                      scales: str = "dual"):
     """R payloads (uint8 CUDA tensors, same n and params) -> requantised sum payload."""
     import torch
     R = len(payloads)
     ptrs = (ctypes.c_void_p * max(R, 1))(*[_dev(p, "payload").value for p in payloads])
     if out is None:
-        out = torch.empty(payload_bytes(n, group, fwht), dtype=torch.uint8,
+        out = torch.empty(payload_bytes(n, group, fwht, scales), dtype=torch.uint8,
                           device=payloads[0].device)
-    p = _lib.params(group, fwht)
+    p = _lib.params(group, fwht, scales=scales)
     st = _lib.lib().fp4q_reduce_requantize(ctypes.cast(ptrs, ctypes.c_void_p), R, int(n),
                                            _dev(out, "out"), ctypes.byref(p),
                                            _stream(stream, out.device))

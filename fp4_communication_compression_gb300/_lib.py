@@ -38,8 +38,12 @@ class Fp4qError(RuntimeError):
         self.status = status
 
 
+SCALES = {"dual": 0, "e8m0": 1}   # fp4q_params.scales: FP4Q_SCALES_DUAL, FP4Q_SCALES_E8M0
+
+
 class Params(ctypes.Structure):
-    _fields_ = [("group", ctypes.c_int32), ("block", ctypes.c_int32), ("fwht", ctypes.c_int32)]
+    _fields_ = [("group", ctypes.c_int32), ("block", ctypes.c_int32), ("fwht", ctypes.c_int32),
+                ("scales", ctypes.c_int32)]
 
 
 def build(force: bool = False, nvcc: str = "nvcc") -> str:
@@ -95,8 +99,13 @@ def lib():
         return L
 
 
-def params(group: int = 16, fwht: int = 1, block: int = 256) -> Params:
-    return Params(group, block, fwht)
+def params(group: int | None = None, fwht: int = 1, block: int = 256, scales: str = "dual") -> Params:
+    """fp4q_params; group None means 16 for dual scales and 32 for E8M0 scales. An unknown
+    scales name maps to -1, which the library rejects (FP4Q_ERR_PARAM)."""
+    sc = SCALES.get(scales, -1)
+    if group is None:
+        group = 32 if sc == 1 else 16
+    return Params(int(group), int(block), int(fwht), sc)
 
 
 def status_string(status: int) -> str:

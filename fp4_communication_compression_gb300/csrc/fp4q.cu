@@ -344,6 +344,61 @@ __device__ __forceinline__ void quantize(const Rows v, Quant& o) {
   }
 }
 
+// Microscaled quantisation (scales = e8m0, groups of 32 = two rows; rows in layout A if
+// !LB, layout B if LB): per group X = 2^(floor(log2 amax) - 2), stored as the E8M0 code
+// max(E - 2, 0) where E is the biased exponent field of amax (subnormal and zero maxima all
+// clamp to code 0, X = 2^-127); q = y * 2^(127 - code), an exact power-of-two scaling that
+// rounds like y / X; code = E2M1(q). The values are the normalised transform y.
+template <bool LB>
+__device__ __forceinline__ void quantize_mx(const Rows v, Quant& o) {
+  float am[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float a[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      a[2 * j] = fabsf(v[k][j].x);
+      a[2 * j + 1] = fabsf(v[k][j].y);
+    }
+    const float m0 = max3(a[0], a[1], a[2]), m1 = max3(a[3], a[4], a[5]), m2 = max3(a[6], a[7], a[8]);
+    const float m3 = max3(a[9], a[10], a[11]), m4 = max3(a[12], a[13], a[14]);
+    am[k] = max3(max3(m0, m1, m2), fmaxf(m3, m4), a[15]);
+  }
+  // a group is two consecutive rows: inside the lane in layout A, across lanes b, b^1 in B
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float other = LB ? __shfl_xor_sync(kFull, am[k], 1) : am[k ^ 1];
+    am[k] = fmaxf(am[k], other);
+  }
+  uint32_t sg = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int E = (int)(__float_as_uint(am[k]) >> 23);
+    const uint32_t c = (uint32_t)(E > 2 ? E - 2 : 0);
+    sg |= c << (8 * k);
+    o.S[k] = __uint_as_float(c ? c << 23 : 0x00400000u);
+    const float m = __uint_as_float((254u - c) << 23);
+    const float2 iv = make_float2(m, m);
+    o.code[k][0] = e2m1_pack8(mul2(v[k][0], iv), mul2(v[k][1], iv), mul2(v[k][2], iv), mul2(v[k][3], iv));
+    o.code[k][1] = e2m1_pack8(mul2(v[k][4], iv), mul2(v[k][5], iv), mul2(v[k][6], iv), mul2(v[k][7], iv));
+  }
+  o.sg = sg;
+  o.sb = 0.0f;
+}
+
+// Value of an E8M0 scale code: 2^(code - 127) (code 0 is the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_value(uint32_t c) { return __uint_as_float(c ? c << 23 : 0x00400000u); }
+
+// Multiply every value of the lane's rows by 1/16 (exact scaling of the unnormalised
+// transform back to y, rounded as the contract's final step rounds it).
+__device__ __forceinline__ void scale_rows_16th(Rows v) {
+  const float2 s = make_float2(0.0625f, 0.0625f);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[k][j] = mul2(v[k][j], s);
+}
+
 // Decode the lane's 4 rows from codes and per-row scales: x~ = grid(code) * S.
 // A packed mul.rn.f32x2 whose product feeds a packed add was observed to be fused into an
 // FMA by the toolchain (even with .rn and --fmad=false), which breaks bit parity in the sums
@@ -383,18 +438,18 @@ __device__ __forceinline__ void scale_by_16th(float S[4]) {
 struct Payload {
   uint8_t* codes;      // n/2 bytes
   uint8_t* gsc;        // n/G bytes (+ padding to 16)
-  float* bsc;          // n/256 floats
+  float* bsc;          // n/256 floats (NULL for the microscaled variant)
   int64_t nb;          // number of blocks
 };
 
 __host__ __device__ inline int64_t pad16(int64_t b) { return (b + 15) / 16 * 16; }
 
-__host__ __device__ inline Payload payload_of(void* base, int64_t n, int G) {
+__host__ __device__ inline Payload payload_of(void* base, int64_t n, int G, bool mx = false) {
   uint8_t* p = static_cast<uint8_t*>(base);
   Payload s;
   s.codes = p;
   s.gsc = p + n / 2;
-  s.bsc = reinterpret_cast<float*>(p + n / 2 + pad16(n / G));
+  s.bsc = mx ? nullptr : reinterpret_cast<float*>(p + n / 2 + pad16(n / G));
   s.nb = n / 256;
   return s;
 }
@@ -404,7 +459,7 @@ template <bool LB>
 __device__ __forceinline__ int row_of(int l4, int k) { return LB ? l4 + 4 * k : 4 * l4 + k; }
 
 // Store the lane's part of a quantised block (block index gb).
-template <int G, bool LB>
+template <int G, bool LB, bool MX = false>
 __device__ __forceinline__ void store_block(const Payload& P, int64_t gb, int l4, const Quant& q) {
   if (LB) {
     // rows l4 + 4k: four separate 8-byte pieces
@@ -439,7 +494,7 @@ __device__ __forceinline__ void store_block(const Payload& P, int64_t gb, int l4
     }
   }
   if (l4 == 0) {
-    P.bsc[gb] = q.sb;
+    if (!MX) P.bsc[gb] = q.sb;
     // G = 32 with an odd block count: the group-scale segment ends 8 bytes short of a
     // 16-byte boundary; the last block zeroes that padding
     if (G == 32 && (P.nb & 1) && gb == P.nb - 1)
@@ -466,7 +521,7 @@ __device__ __forceinline__ void pay_zero(PayRaw& r) {
   r.sb = 0.0f;
 }
 
-template <int G, bool LB>
+template <int G, bool LB, bool MX = false>
 __device__ __forceinline__ void pay_load(const Payload& P, int64_t gb, int l4, PayRaw& r) {
   if (LB) {
 #pragma unroll
@@ -496,11 +551,11 @@ __device__ __forceinline__ void pay_load(const Payload& P, int64_t gb, int l4, P
       r.g[0] = __ldg(reinterpret_cast<const uint16_t*>(P.gsc + gb * 8 + 2 * l4));
     }
   }
-  r.sb = __ldg(P.bsc + gb);
+  r.sb = MX ? 0.0f : __ldg(P.bsc + gb);
 }
 
 // Decode scale S = value(s_g) * s_b of each of the lane's 4 rows.
-template <int G, bool LB>
+template <int G, bool LB, bool MX = false>
 __device__ __forceinline__ void pay_scales(const PayRaw& r, int l4, float S[4]) {
   uint32_t sg;   // row k's group-scale code in byte k
   if (G == 16) {
@@ -522,6 +577,11 @@ __device__ __forceinline__ void pay_scales(const PayRaw& r, int l4, float S[4]) 
       // rows 4 l4 + {0,1} form group 2 l4, rows 4 l4 + {2,3} group 2 l4 + 1
       sg = (r.g[0] & 0xffu) * 0x0101u | ((r.g[0] >> 8) & 0xffu) * 0x01010000u;
     }
+  }
+  if (MX) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) S[k] = e8m0_value((sg >> (8 * k)) & 0xffu);
+    return;
   }
   const float2 s01 = e4m3x2_to_f2(sg & 0xffffu), s23 = e4m3x2_to_f2(sg >> 16);
   S[0] = __fmul_rn(s01.x, r.sb);
@@ -821,7 +881,7 @@ __device__ __forceinline__ void staging_store(const CUtensorMap* map, int lines,
 }
 
 // K1: compress. x (bfloat16, n) -> payload. Input tiles arrive by TMA.
-template <int G, int FWHT>
+template <int G, int FWHT, bool MX>
 __global__ void __launch_bounds__(kCompressWarps * 32, kCompressCtas)
 compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T) {
   extern __shared__ uint8_t smem_raw[];
@@ -851,11 +911,16 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
       transpose<true>(v, xa);
       rows_bfly(v, 1);             // h = 64
       rows_bfly(v, 2);             // h = 128
-      quantize<G, true, true>(v, q);
-      if (valid) store_block<G, true>(P, gb, l4, q);
+      if (MX) {
+        scale_rows_16th(v);
+        quantize_mx<true>(v, q);
+      } else {
+        quantize<G, true, true>(v, q);
+      }
+      if (valid) store_block<G, true, MX>(P, gb, l4, q);
     } else {
-      quantize<G, false, false>(v, q);
-      if (valid) store_block<G, false>(P, gb, l4, q);
+      if (MX) quantize_mx<false>(v, q); else quantize<G, false, false>(v, q);
+      if (valid) store_block<G, false, MX>(P, gb, l4, q);
     }
   }
 }
@@ -863,7 +928,7 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
 // K2: decompress-accumulate. payload -> dst (dtype DT), dst = BETA ? dst + x^ : x^.
 // The payload of the next tile is prefetched into registers; dst tiles are read (BETA) and
 // written through the swizzled shared staging buffer by TMA.
-template <int G, int FWHT, int DT, int BETA>
+template <int G, int FWHT, int DT, int BETA, bool MX>
 __global__ void __launch_bounds__(kDecompressWarps * 32, kDecompressCtas)
 decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop T) {
   constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
@@ -883,13 +948,13 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
   const int64_t t0 = warp_global<kDecompressWarps>(), W = warp_count<kDecompressWarps>();
   if (BETA) pipe.start(ws.stage0, ws.bar0, t0, W, T.tiles, lane, issue);
   PayRaw cur, nxt;
-  if (t0 < T.tiles && t0 * kTileBlocks + blk < T.nb) pay_load<G, LB>(P, t0 * kTileBlocks + blk, l4, cur);
+  if (t0 < T.tiles && t0 * kTileBlocks + blk < T.nb) pay_load<G, LB, MX>(P, t0 * kTileBlocks + blk, l4, cur);
   else pay_zero(cur);
   for (int64_t t = t0; t < T.tiles; t += W) {
     const int64_t tn = t + W, gbn = tn * kTileBlocks + blk;
-    if (tn < T.tiles && gbn < T.nb) pay_load<G, LB>(P, gbn, l4, nxt); else pay_zero(nxt);
+    if (tn < T.tiles && gbn < T.nb) pay_load<G, LB, MX>(P, gbn, l4, nxt); else pay_zero(nxt);
     float S[4];
-    pay_scales<G, LB>(cur, l4, S);
+    pay_scales<G, LB, MX>(cur, l4, S);
     if (FWHT) scale_by_16th(S);
     Rows v;
     dequantize(cur.code, S, v, T.negzero);
@@ -926,7 +991,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
 }
 
 // K3: fused roundtrip. x (bfloat16) -> y = bf16(decode(compress(x))), no payload.
-template <int G, int FWHT>
+template <int G, int FWHT, bool MX>
 __global__ void __launch_bounds__(kRoundtripWarps * 32, kRoundtripCtas)
 roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap, TileLoop T) {
   extern __shared__ uint8_t smem_raw[];
@@ -956,7 +1021,12 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       transpose<true>(v, xa);
       rows_bfly(v, 1);
       rows_bfly(v, 2);
-      quantize<G, true, true>(v, q);
+      if (MX) {
+        scale_rows_16th(v);
+        quantize_mx<true>(v, q);
+      } else {
+        quantize<G, true, true>(v, q);
+      }
       scale_by_16th(q.S);
       dequantize(q.code, q.S, v, T.negzero);
       rows_bfly(v, 2);
@@ -966,7 +1036,7 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       rows_bfly(v, 1);
       level1_inv(v);
     } else {
-      quantize<G, false, false>(v, q);
+      if (MX) quantize_mx<false>(v, q); else quantize<G, false, false>(v, q);
       dequantize(q.code, q.S, v, T.negzero);
       staging_free(lane);
     }
@@ -1004,7 +1074,7 @@ struct ReduceCfg {
   static constexpr int kCtaBytes = kReduceWarps * kRegion + 128;
 };
 
-template <int G, int R>
+template <int G, int R, bool MX>
 __global__ void __launch_bounds__(kReduceWarps * 32, kReduceCtas)
 reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
   typedef ReduceCfg<R> C;
@@ -1029,7 +1099,7 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
     const int64_t left = T.nb - t * kTileBlocks;
     const uint32_t nblk = (uint32_t)(left < kTileBlocks ? left : kTileBlocks);
     const uint32_t cbytes = nblk * 128u, gbytes = (nblk * gs_per_block + 15u) & ~15u;
-    const uint32_t sbytes = (nblk * 4u) & ~15u;
+    const uint32_t sbytes = MX ? 0u : (nblk * 4u) & ~15u;
     // arm the barrier for all R ranks before any of their copies is issued
     if (lane == 0) mbar_expect_tx(bar, (uint32_t)R * (cbytes + gbytes + sbytes));
     __syncwarp();
@@ -1048,7 +1118,7 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
     const bool valid = gb < T.nb;
     // a block scale outside the bulk-copied whole 16-byte units of the last tile
     const int64_t left = T.nb - t * kTileBlocks;
-    const bool direct_sb = valid && left < kTileBlocks && blk >= (int)(left & ~3);
+    const bool direct_sb = !MX && valid && left < kTileBlocks && blk >= (int)(left & ~3);
     if (!pipe.wait()) return;
     Rows z;
 #pragma unroll
@@ -1061,9 +1131,9 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
       raw.code[2][0] = c1.x; raw.code[2][1] = c1.y; raw.code[3][0] = c1.z; raw.code[3][1] = c1.w;
       raw.g[0] = G == 16 ? lds32(b + 1024u + (uint32_t)(blk * 16 + 4 * l4))
                          : lds16(b + 1024u + (uint32_t)(blk * 8 + 2 * l4));
-      raw.sb = direct_sb ? __ldg(in.bsc[r] + gb) : __uint_as_float(lds32(b + 1152u + (uint32_t)(4 * blk)));
+      raw.sb = MX ? 0.0f : direct_sb ? __ldg(in.bsc[r] + gb) : __uint_as_float(lds32(b + 1152u + (uint32_t)(4 * blk)));
       float S[4];
-      pay_scales<G, false>(raw, l4, S);
+      pay_scales<G, false, MX>(raw, l4, S);
       if (r == 0) {
         dequantize(raw.code, S, z, T.negzero);
       } else {
@@ -1077,8 +1147,8 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
     }
     pipe.refill(lane, issue);
     Quant q;
-    quantize<G, false, false>(z, q);
-    if (valid) store_block<G, false>(out, gb, l4, q);
+    if (MX) quantize_mx<false>(z, q); else quantize<G, false, false>(z, q);
+    if (valid) store_block<G, false, MX>(out, gb, l4, q);
   }
 }
 
@@ -1215,13 +1285,16 @@ bool line_map(CUtensorMap* m, const void* ptr, int64_t n, bool f32) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-fp4q_status check_params(const fp4q_params* p, int& G, int& fwht) {
-  fp4q_params d = {FP4Q_GROUP_DEFAULT, FP4Q_BLOCK, 1};
+fp4q_status check_params(const fp4q_params* p, int& G, int& fwht, bool& mx) {
+  fp4q_params d = {FP4Q_GROUP_DEFAULT, FP4Q_BLOCK, 1, FP4Q_SCALES_DUAL};
   if (p) d = *p;
-  if ((d.group != 16 && d.group != 32) || d.block != FP4Q_BLOCK || (d.fwht != 0 && d.fwht != 1))
+  if ((d.group != 16 && d.group != 32) || d.block != FP4Q_BLOCK || (d.fwht != 0 && d.fwht != 1) ||
+      (d.scales != FP4Q_SCALES_DUAL && d.scales != FP4Q_SCALES_E8M0) ||
+      (d.scales == FP4Q_SCALES_E8M0 && d.group != 32))
     return FP4Q_ERR_PARAM;
   G = d.group;
   fwht = d.fwht;
+  mx = d.scales == FP4Q_SCALES_E8M0;
   return FP4Q_OK;
 }
 
@@ -1241,40 +1314,40 @@ TileLoop tiles_of(int64_t n) {
   return T;
 }
 
-template <int G, int F>
+template <int G, int F, bool MX>
 fp4q_status launch_compress(const void* x, int64_t n, void* payload, cudaStream_t s) {
   TileLoop T = tiles_of(n);
   CUtensorMap xm;
   if (!line_map(&xm, x, n, false)) return FP4Q_ERR_CUDA;
-  auto k = compress_kernel<G, F>;
+  auto k = compress_kernel<G, F, MX>;
   Launch L;
   fp4q_status st = plan(k, kCompressWarps, WarpSmemLayout<kCompressWarps, kCompressStages, 4096>::kCtaBytes,
                         T.tiles, L);
   if (st != FP4Q_OK) return st;
-  return launch_pdl(k, L, kCompressWarps * 32, s, xm, payload_of(payload, n, G), T);
+  return launch_pdl(k, L, kCompressWarps * 32, s, xm, payload_of(payload, n, G, MX), T);
 }
 
-template <int G, int F, int DT, int B>
+template <int G, int F, int DT, int B, bool MX>
 fp4q_status launch_decompress(const void* payload, int64_t n, void* dst, cudaStream_t s) {
   TileLoop T = tiles_of(n);
   CUtensorMap dm;
   if (!line_map(&dm, dst, n, DT == FP4Q_F32)) return FP4Q_ERR_CUDA;
-  auto k = decompress_kernel<G, F, DT, B>;
+  auto k = decompress_kernel<G, F, DT, B, MX>;
   constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
   Launch L;
   fp4q_status st = plan(k, kDecompressWarps,
                         WarpSmemLayout<kDecompressWarps, kDecompressStages, B ? TB : 0>::kCtaBytes, T.tiles, L,
                         kDecompressGridCtas);
   if (st != FP4Q_OK) return st;
-  return launch_pdl(k, L, kDecompressWarps * 32, s, dm, payload_of(const_cast<void*>(payload), n, G), T);
+  return launch_pdl(k, L, kDecompressWarps * 32, s, dm, payload_of(const_cast<void*>(payload), n, G, MX), T);
 }
 
-template <int G, int F>
+template <int G, int F, bool MX>
 fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) {
   TileLoop T = tiles_of(n);
   CUtensorMap xm, ym;
   if (!line_map(&xm, x, n, false) || !line_map(&ym, y, n, false)) return FP4Q_ERR_CUDA;
-  auto k = roundtrip_kernel<G, F>;
+  auto k = roundtrip_kernel<G, F, MX>;
   Launch L;
   fp4q_status st = plan(k, kRoundtripWarps, WarpSmemLayout<kRoundtripWarps, kRoundtripStages, 4096>::kCtaBytes,
                         T.tiles, L);
@@ -1282,40 +1355,54 @@ fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) 
   return launch_pdl(k, L, kRoundtripWarps * 32, s, xm, ym, T);
 }
 
-template <int G, int R>
+template <int G, int R, bool MX>
 fp4q_status launch_reduce_r(const RankPtrs& in, int64_t n, void* out, cudaStream_t s) {
   TileLoop T = tiles_of(n);
-  auto k = reduce_kernel<G, R>;
+  auto k = reduce_kernel<G, R, MX>;
   Launch L;
   fp4q_status st = plan(k, kReduceWarps, ReduceCfg<R>::kCtaBytes, T.tiles, L);
   if (st != FP4Q_OK) return st;
-  return launch_pdl(k, L, kReduceWarps * 32, s, in, payload_of(out, n, G), T);
+  return launch_pdl(k, L, kReduceWarps * 32, s, in, payload_of(out, n, G, MX), T);
 }
 
-template <int G>
+template <int G, bool MX>
 fp4q_status launch_reduce(const void* const* payloads, int R, int64_t n, void* out, cudaStream_t s) {
   RankPtrs in;
   memset(&in, 0, sizeof(in));
   for (int r = 0; r < R; ++r) {
-    const Payload p = payload_of(const_cast<void*>(payloads[r]), n, G);
+    const Payload p = payload_of(const_cast<void*>(payloads[r]), n, G, MX);
     in.codes[r] = p.codes;
     in.gsc[r] = p.gsc;
     in.bsc[r] = p.bsc;
   }
   switch (R) {
-    case 1: return launch_reduce_r<G, 1>(in, n, out, s);
-    case 2: return launch_reduce_r<G, 2>(in, n, out, s);
-    case 3: return launch_reduce_r<G, 3>(in, n, out, s);
-    case 4: return launch_reduce_r<G, 4>(in, n, out, s);
-    case 5: return launch_reduce_r<G, 5>(in, n, out, s);
-    case 6: return launch_reduce_r<G, 6>(in, n, out, s);
-    case 7: return launch_reduce_r<G, 7>(in, n, out, s);
-    default: return launch_reduce_r<G, 8>(in, n, out, s);
+    case 1: return launch_reduce_r<G, 1, MX>(in, n, out, s);
+    case 2: return launch_reduce_r<G, 2, MX>(in, n, out, s);
+    case 3: return launch_reduce_r<G, 3, MX>(in, n, out, s);
+    case 4: return launch_reduce_r<G, 4, MX>(in, n, out, s);
+    case 5: return launch_reduce_r<G, 5, MX>(in, n, out, s);
+    case 6: return launch_reduce_r<G, 6, MX>(in, n, out, s);
+    case 7: return launch_reduce_r<G, 7, MX>(in, n, out, s);
+    default: return launch_reduce_r<G, 8, MX>(in, n, out, s);
   }
 }
 
-size_t payload_bytes_of(int64_t n, int G) {
-  return (size_t)(n / 2 + pad16(n / G) + 4 * (n / FP4Q_BLOCK));
+size_t payload_bytes_of(int64_t n, int G, bool mx) {
+  return (size_t)(n / 2 + pad16(n / G) + (mx ? 0 : 4 * (n / FP4Q_BLOCK)));
+}
+
+template <int G, bool MX>
+fp4q_status dispatch_decompress(int key, const void* payload, int64_t n, void* dst, cudaStream_t s) {
+  switch (key) {
+    case 0: return launch_decompress<G, 0, FP4Q_BF16, 0, MX>(payload, n, dst, s);
+    case 1: return launch_decompress<G, 0, FP4Q_BF16, 1, MX>(payload, n, dst, s);
+    case 2: return launch_decompress<G, 0, FP4Q_F32, 0, MX>(payload, n, dst, s);
+    case 3: return launch_decompress<G, 0, FP4Q_F32, 1, MX>(payload, n, dst, s);
+    case 4: return launch_decompress<G, 1, FP4Q_BF16, 0, MX>(payload, n, dst, s);
+    case 5: return launch_decompress<G, 1, FP4Q_BF16, 1, MX>(payload, n, dst, s);
+    case 6: return launch_decompress<G, 1, FP4Q_F32, 0, MX>(payload, n, dst, s);
+    default: return launch_decompress<G, 1, FP4Q_F32, 1, MX>(payload, n, dst, s);
+  }
 }
 
 }  // namespace
@@ -1324,87 +1411,81 @@ extern "C" {
 
 size_t fp4q_payload_bytes(int64_t n, const fp4q_params* params) {
   int G, f;
-  if (!size_ok(n) || check_params(params, G, f) != FP4Q_OK) return 0;
-  return payload_bytes_of(n, G);
+  bool mx;
+  if (!size_ok(n) || check_params(params, G, f, mx) != FP4Q_OK) return 0;
+  return payload_bytes_of(n, G, mx);
 }
 
 size_t fp4q_gscale_offset(int64_t n, const fp4q_params* params) {
   int G, f;
-  if (!size_ok(n) || check_params(params, G, f) != FP4Q_OK) return 0;
+  bool mx;
+  if (!size_ok(n) || check_params(params, G, f, mx) != FP4Q_OK) return 0;
   return (size_t)(n / 2);
 }
 
 size_t fp4q_bscale_offset(int64_t n, const fp4q_params* params) {
   int G, f;
-  if (!size_ok(n) || check_params(params, G, f) != FP4Q_OK) return 0;
+  bool mx;
+  if (!size_ok(n) || check_params(params, G, f, mx) != FP4Q_OK) return 0;
   return (size_t)(n / 2 + pad16(n / G));
 }
 
 fp4q_status fp4q_compress(const void* x_bf16, int64_t n, void* payload, const fp4q_params* params,
                           void* stream) {
   int G, F;
-  fp4q_status st = check_params(params, G, F);
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
   if (st != FP4Q_OK) return st;
   if (!x_bf16 || !payload) return FP4Q_ERR_NULL;
   if (!size_ok(n)) return FP4Q_ERR_SIZE;
   if (!aligned16(x_bf16) || !aligned16(payload)) return FP4Q_ERR_ALIGN;
-  if (overlap(x_bf16, (size_t)n * 2, payload, payload_bytes_of(n, G))) return FP4Q_ERR_OVERLAP;
+  if (overlap(x_bf16, (size_t)n * 2, payload, payload_bytes_of(n, G, MX))) return FP4Q_ERR_OVERLAP;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (G == 16) return F ? launch_compress<16, 1>(x_bf16, n, payload, s) : launch_compress<16, 0>(x_bf16, n, payload, s);
-  return F ? launch_compress<32, 1>(x_bf16, n, payload, s) : launch_compress<32, 0>(x_bf16, n, payload, s);
+  if (MX) return F ? launch_compress<32, 1, true>(x_bf16, n, payload, s) : launch_compress<32, 0, true>(x_bf16, n, payload, s);
+  if (G == 16) return F ? launch_compress<16, 1, false>(x_bf16, n, payload, s) : launch_compress<16, 0, false>(x_bf16, n, payload, s);
+  return F ? launch_compress<32, 1, false>(x_bf16, n, payload, s) : launch_compress<32, 0, false>(x_bf16, n, payload, s);
 }
 
 fp4q_status fp4q_decompress_accumulate(const void* payload, int64_t n, void* dst, fp4q_dtype dtype,
                                        int32_t beta, const fp4q_params* params, void* stream) {
   int G, F;
-  fp4q_status st = check_params(params, G, F);
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
   if (st != FP4Q_OK) return st;
   if ((dtype != FP4Q_BF16 && dtype != FP4Q_F32) || (beta != 0 && beta != 1)) return FP4Q_ERR_PARAM;
   if (!payload || !dst) return FP4Q_ERR_NULL;
   if (!size_ok(n)) return FP4Q_ERR_SIZE;
   if (!aligned16(payload) || !aligned16(dst)) return FP4Q_ERR_ALIGN;
   const size_t dbytes = (size_t)n * (dtype == FP4Q_BF16 ? 2 : 4);
-  if (overlap(payload, payload_bytes_of(n, G), dst, dbytes)) return FP4Q_ERR_OVERLAP;
+  if (overlap(payload, payload_bytes_of(n, G, MX), dst, dbytes)) return FP4Q_ERR_OVERLAP;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int key = (G == 32) * 8 + F * 4 + (dtype == FP4Q_F32) * 2 + beta;
-  switch (key) {
-    case 0: return launch_decompress<16, 0, FP4Q_BF16, 0>(payload, n, dst, s);
-    case 1: return launch_decompress<16, 0, FP4Q_BF16, 1>(payload, n, dst, s);
-    case 2: return launch_decompress<16, 0, FP4Q_F32, 0>(payload, n, dst, s);
-    case 3: return launch_decompress<16, 0, FP4Q_F32, 1>(payload, n, dst, s);
-    case 4: return launch_decompress<16, 1, FP4Q_BF16, 0>(payload, n, dst, s);
-    case 5: return launch_decompress<16, 1, FP4Q_BF16, 1>(payload, n, dst, s);
-    case 6: return launch_decompress<16, 1, FP4Q_F32, 0>(payload, n, dst, s);
-    case 7: return launch_decompress<16, 1, FP4Q_F32, 1>(payload, n, dst, s);
-    case 8: return launch_decompress<32, 0, FP4Q_BF16, 0>(payload, n, dst, s);
-    case 9: return launch_decompress<32, 0, FP4Q_BF16, 1>(payload, n, dst, s);
-    case 10: return launch_decompress<32, 0, FP4Q_F32, 0>(payload, n, dst, s);
-    case 11: return launch_decompress<32, 0, FP4Q_F32, 1>(payload, n, dst, s);
-    case 12: return launch_decompress<32, 1, FP4Q_BF16, 0>(payload, n, dst, s);
-    case 13: return launch_decompress<32, 1, FP4Q_BF16, 1>(payload, n, dst, s);
-    case 14: return launch_decompress<32, 1, FP4Q_F32, 0>(payload, n, dst, s);
-    default: return launch_decompress<32, 1, FP4Q_F32, 1>(payload, n, dst, s);
-  }
+  const int key = F * 4 + (dtype == FP4Q_F32) * 2 + beta;
+  if (MX) return dispatch_decompress<32, true>(key, payload, n, dst, s);
+  return G == 16 ? dispatch_decompress<16, false>(key, payload, n, dst, s)
+                 : dispatch_decompress<32, false>(key, payload, n, dst, s);
 }
 
 fp4q_status fp4q_roundtrip(const void* x_bf16, int64_t n, void* y_bf16, const fp4q_params* params,
                            void* stream) {
   int G, F;
-  fp4q_status st = check_params(params, G, F);
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
   if (st != FP4Q_OK) return st;
   if (!x_bf16 || !y_bf16) return FP4Q_ERR_NULL;
   if (!size_ok(n)) return FP4Q_ERR_SIZE;
   if (!aligned16(x_bf16) || !aligned16(y_bf16)) return FP4Q_ERR_ALIGN;
   if (overlap(x_bf16, (size_t)n * 2, y_bf16, (size_t)n * 2)) return FP4Q_ERR_OVERLAP;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (G == 16) return F ? launch_roundtrip<16, 1>(x_bf16, n, y_bf16, s) : launch_roundtrip<16, 0>(x_bf16, n, y_bf16, s);
-  return F ? launch_roundtrip<32, 1>(x_bf16, n, y_bf16, s) : launch_roundtrip<32, 0>(x_bf16, n, y_bf16, s);
+  if (MX) return F ? launch_roundtrip<32, 1, true>(x_bf16, n, y_bf16, s) : launch_roundtrip<32, 0, true>(x_bf16, n, y_bf16, s);
+  if (G == 16) return F ? launch_roundtrip<16, 1, false>(x_bf16, n, y_bf16, s) : launch_roundtrip<16, 0, false>(x_bf16, n, y_bf16, s);
+  return F ? launch_roundtrip<32, 1, false>(x_bf16, n, y_bf16, s) : launch_roundtrip<32, 0, false>(x_bf16, n, y_bf16, s);
 }
 
 fp4q_status fp4q_reduce_requantize(const void* const* payloads, int32_t R, int64_t n, void* out_payload,
                                    const fp4q_params* params, void* stream) {
   int G, F;
-  fp4q_status st = check_params(params, G, F);
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
   if (st != FP4Q_OK) return st;
   if (R < 1 || R > FP4Q_MAX_RANKS) return FP4Q_ERR_PARAM;
   if (!payloads || !out_payload) return FP4Q_ERR_NULL;
@@ -1414,11 +1495,13 @@ fp4q_status fp4q_reduce_requantize(const void* const* payloads, int32_t R, int64
   if (!aligned16(out_payload)) return FP4Q_ERR_ALIGN;
   for (int r = 0; r < R; ++r)
     if (!aligned16(payloads[r])) return FP4Q_ERR_ALIGN;
-  const size_t pb = payload_bytes_of(n, G);
+  const size_t pb = payload_bytes_of(n, G, MX);
   for (int r = 0; r < R; ++r)
     if (overlap(payloads[r], pb, out_payload, pb)) return FP4Q_ERR_OVERLAP;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return G == 16 ? launch_reduce<16>(payloads, R, n, out_payload, s) : launch_reduce<32>(payloads, R, n, out_payload, s);
+  if (MX) return launch_reduce<32, true>(payloads, R, n, out_payload, s);
+  return G == 16 ? launch_reduce<16, false>(payloads, R, n, out_payload, s)
+                 : launch_reduce<32, false>(payloads, R, n, out_payload, s);
 }
 
 fp4q_status fp4q_fault_flags(uint32_t* flags, int32_t clear) {
@@ -1445,13 +1528,13 @@ const char* fp4q_status_string(fp4q_status status) {
     case FP4Q_ERR_NULL: return "null pointer";
     case FP4Q_ERR_SIZE: return "n must be a positive multiple of 256 below 2^37";
     case FP4Q_ERR_ALIGN: return "pointer not 16-byte aligned";
-    case FP4Q_ERR_PARAM: return "invalid parameter (group, block, fwht, R, dtype, beta or polls)";
+    case FP4Q_ERR_PARAM: return "invalid parameter (group, block, fwht, scales, R, dtype, beta or polls)";
     case FP4Q_ERR_OVERLAP: return "output overlaps an input";
     case FP4Q_ERR_CUDA: return "CUDA runtime error or failed launch";
   }
   return "unknown status";
 }
 
-int32_t fp4q_version(void) { return 200; }
+int32_t fp4q_version(void) { return 300; }
 
 }  // extern "C"

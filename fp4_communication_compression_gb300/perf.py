@@ -5,7 +5,8 @@
 
 Each kernel is timed alone with CUDA events on the launching stream, after an L2 flush
 (a write of a buffer larger than L2 followed by a read of another one), and reported as
-algorithmic GB/s (the bytes the kernel must move, G = 16) and as a fraction of the measured
+algorithmic GB/s (the bytes the kernel must move, G = 16; the *_mx kernels use the E8M0
+variant, group 32) and as a fraction of the measured
 HBM copy bandwidth in MEASURED_PEAKS.json when that file is present. Inputs are N(0,1)
 bfloat16 tensors made on the device (timing only; parity is the tests' business).
 """
@@ -21,6 +22,7 @@ import torch
 import fp4_communication_compression_gb300 as fq
 
 PAYLOAD = 0.5 + 1 / 16 + 4 / 256          # bytes per element of a G = 16 payload
+PAYLOAD_MX = 0.5 + 1 / 32                 # bytes per element of an E8M0 (group 32) payload
 ALG_BYTES = {
     "compress": 2 + PAYLOAD,
     "decompress_bf16_b1": PAYLOAD + 4,
@@ -31,6 +33,10 @@ ALG_BYTES = {
     "reduce_r4": 5 * PAYLOAD,
     "reduce_r8": 9 * PAYLOAD,
     "copy_bf16": 4.0,
+    "compress_mx": 2 + PAYLOAD_MX,
+    "decompress_mx_bf16_b1": PAYLOAD_MX + 4,
+    "roundtrip_mx": 4.0,
+    "reduce_mx_r4": 5 * PAYLOAD_MX,
 }
 
 
@@ -45,7 +51,7 @@ def peak_gbs():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--sizes", type=int, nargs="+", default=[1 << 24, 1 << 26, 1 << 28])
-    ap.add_argument("--kernels", nargs="+", default=list(ALG_BYTES))
+    ap.add_argument("--kernels", nargs="+", default=[k for k in ALG_BYTES if "_mx" not in k])
     ap.add_argument("--iters", type=int, default=30)
     args = ap.parse_args()
     dev = torch.device("cuda:0")
@@ -74,6 +80,9 @@ def main():
         d32 = torch.zeros(n, dtype=torch.float32, device=dev)
         y = torch.empty_like(x)
         out = torch.empty_like(ps[0])
+        mx = any("_mx" in k for k in args.kernels)
+        pm = [fq.compress(x * (r + 1), scales="e8m0") for r in range(4)] if mx else None
+        outm = torch.empty_like(pm[0]) if mx else None
         fns = {
             "compress": lambda: fq.compress(x, payload=ps[0]),
             "decompress_bf16_b1": lambda: fq.decompress_accumulate(ps[0], n, d16, beta=1),
@@ -84,13 +93,17 @@ def main():
             "reduce_r4": lambda: fq.reduce_requantize(ps[:4], n, out=out),
             "reduce_r8": lambda: fq.reduce_requantize(ps[:8], n, out=out),
             "copy_bf16": lambda: y.copy_(x),
+            "compress_mx": lambda: fq.compress(x, payload=pm[0], scales="e8m0"),
+            "decompress_mx_bf16_b1": lambda: fq.decompress_accumulate(pm[0], n, d16, beta=1, scales="e8m0"),
+            "roundtrip_mx": lambda: fq.roundtrip(x, y=y, scales="e8m0"),
+            "reduce_mx_r4": lambda: fq.reduce_requantize(pm[:4], n, out=outm, scales="e8m0"),
         }
         for k in args.kernels:
             t = timed(fns[k])
             gbs = ALG_BYTES[k] * n / t / 1e9
             print(json.dumps({"n": n, "kernel": k, "us": round(t * 1e6, 2), "alg_gbs": round(gbs, 1),
                               "frac_of_peak": None if not peak else round(gbs / peak, 4)}), flush=True)
-        del x, ps, d16, d32, y, out
+        del x, ps, d16, d32, y, out, pm, outm
 
 
 if __name__ == "__main__":

@@ -12,7 +12,8 @@
  *        scaling factors, values are packed two per byte, a fast transform keeps errors
  *        low; the compressed tensors are the ones the tensor-parallel AllReduce exchanges.
  *   [P4] "Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs"
- *        (gist.science), technical summary, problem statement: FP4 elements are E2M1.
+ *        (gist.science), technical summary, problem statement: FP4 elements are E2M1, and
+ *        the microscaled MXFP4 format scales blocks of 32 of them.
  *
  * The pages fix the shape of the method but none of its numbers. This header is the one
  * place where the numbers are fixed; every kernel and the CPU oracle implement exactly
@@ -36,6 +37,12 @@
  *              t_b = s_b * 6.0f; per group of G elements r_g = amax_g / t_b (IEEE div);
  *              s_g = E4M3(r_g): round to nearest, ties to the even code, saturating at
  *              448 (OCP e4m3fn, codes 0x00..0x7E, never 0x7F).
+ *   Scales, microscaled variant (scales = FP4Q_SCALES_E8M0, group 32 only) [P4 problem
+ *            statement: MXFP4 scales blocks of 32 E2M1 elements]: no block scale; per group
+ *            X = 2^(floor(log2 amax_g) - 2), stored as the E8M0 byte e + 127 with the
+ *            exponent e clamped below at -127 (amax_g = 0 and subnormal maxima give byte 0),
+ *            so amax_g / X lies in [4, 8); q = y / X (exact), code as below; decode
+ *            x~ = grid(code) * X. No all-zero guard: a zero keeps its sign (0x0 / 0x8).
  *   Codes.   S_g = float(s_g) * s_b; inv_g = S_g > 0 ? 1.0f / S_g : 0.0f (IEEE);
  *            q = y * inv_g; code = sign(q) << 3 | E2M1(|q|), E2M1 = round to nearest,
  *            ties to the even code, onto {0, 0.5, 1, 1.5, 2, 3, 4, 6} (codes 0..7),
@@ -45,7 +52,7 @@
  *            the low nibble). [P3 "packed two per byte"]
  *   Payload. One contiguous byte buffer, structure of arrays:
  *              [codes: n/2 bytes][group scales: n/G bytes, zero-padded to a multiple of
- *              16][block scales: n/256 x float32, little endian]
+ *              16][block scales: n/256 x float32, little endian; absent for E8M0 scales]
  *            Every segment starts 16-byte aligned when the buffer does. A contiguous range
  *            of blocks can be cut out of each segment.
  *   Decode.  x~ = grid(code) * S_g (signed, FP32); if fwht, the inverse transform: the
@@ -87,6 +94,8 @@ extern "C" {
 #define FP4Q_E4M3_MAX 448.0f        /* largest finite e4m3fn value                      */
 #define FP4Q_E2M1_MAX 6.0f          /* largest E2M1 value                               */
 #define FP4Q_BLOCK_DENOM 2688.0f    /* FP4Q_E4M3_MAX * FP4Q_E2M1_MAX                    */
+#define FP4Q_SCALES_DUAL 0          /* E4M3 group scale x FP32 block scale (default)     */
+#define FP4Q_SCALES_E8M0 1          /* power-of-two E8M0 scale per group of 32          */
 
 typedef enum fp4q_status {
   FP4Q_OK = 0,
@@ -94,7 +103,8 @@ typedef enum fp4q_status {
   FP4Q_ERR_SIZE = 2,     /* n <= 0, n % 256 != 0, or n >= 2^37                          */
   FP4Q_ERR_ALIGN = 3,    /* a data pointer is not 16-byte aligned                       */
   FP4Q_ERR_PARAM = 4,    /* bad params: group not 16/32, block not 256, fwht not 0/1,
-                            R outside [1, 8], unknown dtype, beta not 0/1               */
+                            scales not 0/1 or E8M0 with group != 32, R outside [1, 8],
+                            unknown dtype, beta not 0/1                                 */
   FP4Q_ERR_OVERLAP = 5,  /* an output buffer overlaps an input buffer                   */
   FP4Q_ERR_CUDA = 6      /* a CUDA runtime call or a kernel launch failed               */
 } fp4q_status;
@@ -103,6 +113,7 @@ typedef struct fp4q_params {
   int32_t group;  /* G: 16 (default) or 32 elements per group scale                    */
   int32_t block;  /* must be 256                                                        */
   int32_t fwht;   /* 1: apply the FWHT (default); 0: quantize the raw values            */
+  int32_t scales; /* FP4Q_SCALES_DUAL (default) or FP4Q_SCALES_E8M0 (needs group 32)    */
 } fp4q_params;
 
 typedef enum fp4q_dtype {
@@ -110,8 +121,9 @@ typedef enum fp4q_dtype {
   FP4Q_F32 = 1    /* destination is float32                                             */
 } fp4q_dtype;
 
-/* Bytes of the payload for n elements: n/2 + pad16(n/G) + 4*(n/256).
- * Returns 0 when n or params are invalid. params == NULL means the defaults {16,256,1}. */
+/* Bytes of the payload for n elements: n/2 + pad16(n/G) + 4*(n/256) (dual scales) or
+ * n/2 + pad16(n/32) (E8M0 scales). Returns 0 when n or params are invalid.
+ * params == NULL means the defaults {16, 256, 1, FP4Q_SCALES_DUAL}. */
 size_t fp4q_payload_bytes(int64_t n, const fp4q_params* params);
 
 /* Byte offsets of the group-scale and block-scale segments inside the payload

@@ -53,12 +53,26 @@ def test_payload_layout_matches_oracle(L, n, G):
     assert L.fp4q_bscale_offset(n, ctypes.byref(p)) % 16 == 0
 
 
+@pytest.mark.parametrize("n", [256, 4096, 256 * 17, 1 << 24, 256 * 1001])
+def test_e8m0_payload_layout_matches_oracle(L, n):
+    p = _lib.params(fwht=1, scales="e8m0")
+    assert p.group == 32
+    assert L.fp4q_payload_bytes(n, ctypes.byref(p)) == oracle.payload_bytes(n, scales="e8m0")
+    assert L.fp4q_payload_bytes(n, ctypes.byref(p)) == n // 2 + (n // 32 + 15) // 16 * 16
+    assert L.fp4q_gscale_offset(n, ctypes.byref(p)) == oracle.gscale_offset(n, scales="e8m0")
+    assert L.fp4q_bscale_offset(n, ctypes.byref(p)) == oracle.bscale_offset(n, scales="e8m0")
+
+
 def test_payload_bytes_defaults_and_invalid(L):
     assert L.fp4q_payload_bytes(4096, None) == 2368
     for n in (0, -256, 100, 1 << 37, 1 << 40):
         assert L.fp4q_payload_bytes(n, None) == 0
     for g, b, f in [(8, 256, 1), (16, 128, 1), (16, 256, 2), (64, 256, 0)]:
         assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(g, b, f))) == 0
+    # E8M0 scales need group 32; unknown scale formats are rejected
+    for g, sc in [(16, 1), (32, 2), (32, -1), (16, 7)]:
+        assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(g, 256, 1, sc))) == 0
+    assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(32, 256, 0, 1))) == 2048 + 128
 
 
 # Fake, never dereferenced device addresses: every call below must fail a host check.
@@ -77,7 +91,7 @@ def test_compress_argument_errors(L):
     assert L.fp4q_compress(A, 4096, B + 2, pp, None) == _lib.ERR_ALIGN
     assert L.fp4q_compress(A, 4096, A + 16, pp, None) == _lib.ERR_OVERLAP
     assert L.fp4q_compress(A, 4096, A + 2 * 4096 - 16, pp, None) == _lib.ERR_OVERLAP
-    for bad in [(8, 256, 1), (16, 512, 1), (16, 256, -1), (33, 256, 0)]:
+    for bad in [(8, 256, 1), (16, 512, 1), (16, 256, -1), (33, 256, 0), (16, 256, 1, 1), (32, 256, 1, 3)]:
         assert L.fp4q_compress(A, 4096, B, ctypes.byref(_lib.Params(*bad)), None) == _lib.ERR_PARAM
 
 
