@@ -248,11 +248,12 @@ def reduce_requantize(payloads, n: int, group: int | None = None, want_q: bool =
 
 
 def split_payload(payload: np.ndarray, n: int, group: int | None = None, scales: str = "dual"):
-    """(codes uint8[n/2], gscale uint8[n/G], bscale float32[n/256]) views of a payload (the
-    block scales are empty for scales="e8m0")."""
+    """(codes, group scales, block scales) views of a payload of n elements, each covering
+    ceil(n/256) blocks (the block scales are empty for scales="e8m0")."""
     G, mx = _fmt(group, scales)
+    m = -(-n // BLOCK) * BLOCK          # a last partial block is zero-padded to 256 elements
     g0, b0 = gscale_offset(n, G, scales), bscale_offset(n, G, scales)
-    codes = payload[:n // 2]
-    gsc = payload[g0:g0 + n // G]
-    bsc = payload[b0:b0 + (0 if mx else 4 * (n // BLOCK))].view(np.float32)
+    codes = payload[:m // 2]
+    gsc = payload[g0:g0 + m // G]
+    bsc = payload[b0:b0 + (0 if mx else 4 * (m // BLOCK))].view(np.float32)
     return codes, gsc, bsc

@@ -183,19 +183,26 @@ static int64_t pad16(int64_t b) { return (b + 15) / 16 * 16; }
 static int valid(int64_t n, int G, int mx) {
   if (mx != 0 && mx != 1) return 0;
   if (mx ? G != 32 : (G != 16 && G != 32)) return 0;
-  return n > 0 && n % ORACLE_BLOCK == 0 && n < ((int64_t)1 << 40);
+  return n > 0 && n < ((int64_t)1 << 40);
 }
+
+/* Elements covered by the payload: n rounded up to whole blocks. A last partial block is
+ * zero-padded (the build's reading; the pages say nothing about lengths that are not a
+ * multiple of the block): its missing elements are +0 going in, and the decode writes
+ * only the n real elements back. */
+static int64_t padded(int64_t n) { return (n + ORACLE_BLOCK - 1) / ORACLE_BLOCK * ORACLE_BLOCK; }
 
 /* Payload = [codes n/2 bytes][group scales n/G bytes, padded to 16][block scales n/256
  * float32; absent when mx]. [P3 "values are packed two per byte"; the layout itself is the
  * build's reading, the pages give none] Returns 0 on invalid arguments. */
 int64_t oracle_payload_bytes(int64_t n, int G, int mx) {
   if (!valid(n, G, mx)) return 0;
-  return n / 2 + pad16(n / G) + (mx ? 0 : 4 * (n / ORACLE_BLOCK));
+  const int64_t m = padded(n);
+  return m / 2 + pad16(m / G) + (mx ? 0 : 4 * (m / ORACLE_BLOCK));
 }
-int64_t oracle_gscale_offset(int64_t n, int G, int mx) { return valid(n, G, mx) ? n / 2 : 0; }
+int64_t oracle_gscale_offset(int64_t n, int G, int mx) { return valid(n, G, mx) ? padded(n) / 2 : 0; }
 int64_t oracle_bscale_offset(int64_t n, int G, int mx) {
-  return valid(n, G, mx) ? n / 2 + pad16(n / G) : 0;
+  return valid(n, G, mx) ? padded(n) / 2 + pad16(padded(n) / G) : 0;
 }
 
 /* ---------------------------------------------------------------- one block */
@@ -317,25 +324,30 @@ void oracle_set_threads(int t) {
 int oracle_compress(const uint16_t* x, int64_t n, uint8_t* payload, int G, int fwht, int mx,
                     float* q_out) {
   if (!valid(n, G, mx) || (fwht != 0 && fwht != 1) || !x || !payload) return -1;
-  int64_t nb = n / ORACLE_BLOCK;
+  const int64_t m = padded(n), nb = m / ORACLE_BLOCK;
   uint8_t* codes = payload;
   uint8_t* gsc = payload + oracle_gscale_offset(n, G, mx);
   float* bsc = (float*)(payload + oracle_bscale_offset(n, G, mx));
-  memset(gsc + n / G, 0, (size_t)(pad16(n / G) - n / G));
+  memset(gsc + m / G, 0, (size_t)(pad16(m / G) - m / G));
 #pragma omp parallel for schedule(static)
   for (int64_t b = 0; b < nb; ++b) {
     float y[ORACLE_BLOCK];
     uint8_t code[ORACLE_BLOCK];
     float s_b;
-    for (int i = 0; i < ORACLE_BLOCK; ++i) y[i] = oracle_bf16_to_f32(x[b * ORACLE_BLOCK + i]);
+    for (int i = 0; i < ORACLE_BLOCK; ++i) {
+      const int64_t e = b * ORACLE_BLOCK + i;
+      y[i] = e < n ? oracle_bf16_to_f32(x[e]) : 0.0f;
+    }
     if (fwht) oracle_fwht256(y);
+    float qb[ORACLE_BLOCK];
     if (mx) {
-      quantize_block_mx(y, code, gsc + b * (ORACLE_BLOCK / 32), q_out ? q_out + b * ORACLE_BLOCK : NULL);
+      quantize_block_mx(y, code, gsc + b * (ORACLE_BLOCK / 32), qb);
     } else {
-      quantize_block(y, G, code, gsc + b * (ORACLE_BLOCK / G), &s_b,
-                     q_out ? q_out + b * ORACLE_BLOCK : NULL);
+      quantize_block(y, G, code, gsc + b * (ORACLE_BLOCK / G), &s_b, qb);
       memcpy(&bsc[b], &s_b, 4);
     }
+    if (q_out)
+      for (int i = 0; i < ORACLE_BLOCK && b * ORACLE_BLOCK + i < n; ++i) q_out[b * ORACLE_BLOCK + i] = qb[i];
     pack_block(code, codes + b * (ORACLE_BLOCK / 2));
   }
   return 0;
@@ -366,12 +378,12 @@ int oracle_decompress_accumulate(const uint8_t* payload, int64_t n, void* dst, i
   if (!valid(n, G, mx) || (fwht != 0 && fwht != 1) || (dtype != 0 && dtype != 1) ||
       (beta != 0 && beta != 1) || !payload || !dst)
     return -1;
-  int64_t nb = n / ORACLE_BLOCK;
+  const int64_t nb = padded(n) / ORACLE_BLOCK;
 #pragma omp parallel for schedule(static)
   for (int64_t b = 0; b < nb; ++b) {
     float xh[ORACLE_BLOCK];
     decode_all(payload, n, G, fwht, mx, b, xh);
-    for (int i = 0; i < ORACLE_BLOCK; ++i) {
+    for (int i = 0; i < ORACLE_BLOCK && b * ORACLE_BLOCK + i < n; ++i) {
       int64_t e = b * ORACLE_BLOCK + i;
       if (dtype == 0) {
         uint16_t* d = (uint16_t*)dst;
@@ -407,11 +419,11 @@ int oracle_reduce_requantize(const uint8_t* const* payloads, int R, int64_t n, u
   if (!valid(n, G, mx) || R < 1 || R > ORACLE_MAX_RANKS || !payloads || !out) return -1;
   for (int r = 0; r < R; ++r)
     if (!payloads[r]) return -1;
-  int64_t nb = n / ORACLE_BLOCK;
+  const int64_t m = padded(n), nb = m / ORACLE_BLOCK;
   uint8_t* codes = out;
   uint8_t* gsc = out + oracle_gscale_offset(n, G, mx);
   float* bsc = (float*)(out + oracle_bscale_offset(n, G, mx));
-  memset(gsc + n / G, 0, (size_t)(pad16(n / G) - n / G));
+  memset(gsc + m / G, 0, (size_t)(pad16(m / G) - m / G));
 #pragma omp parallel for schedule(static)
   for (int64_t b = 0; b < nb; ++b) {
     float z[ORACLE_BLOCK], xr[ORACLE_BLOCK];
@@ -422,13 +434,15 @@ int oracle_reduce_requantize(const uint8_t* const* payloads, int R, int64_t n, u
       decode_all(payloads[r], n, G, 0, mx, b, xr);
       for (int i = 0; i < ORACLE_BLOCK; ++i) z[i] = z[i] + xr[i];
     }
+    float qb[ORACLE_BLOCK];
     if (mx) {
-      quantize_block_mx(z, code, gsc + b * (ORACLE_BLOCK / 32), q_out ? q_out + b * ORACLE_BLOCK : NULL);
+      quantize_block_mx(z, code, gsc + b * (ORACLE_BLOCK / 32), qb);
     } else {
-      quantize_block(z, G, code, gsc + b * (ORACLE_BLOCK / G), &s_b,
-                     q_out ? q_out + b * ORACLE_BLOCK : NULL);
+      quantize_block(z, G, code, gsc + b * (ORACLE_BLOCK / G), &s_b, qb);
       memcpy(&bsc[b], &s_b, 4);
     }
+    if (q_out)
+      for (int i = 0; i < ORACLE_BLOCK && b * ORACLE_BLOCK + i < n; ++i) q_out[b * ORACLE_BLOCK + i] = qb[i];
     pack_block(code, codes + b * (ORACLE_BLOCK / 2));
   }
   return 0;

@@ -194,7 +194,8 @@ def test_payload_layout_sizes():
     assert oracle.payload_bytes(256, 32) == 128 + 16 + 4          # 8 scale bytes padded to 16
     assert oracle.bscale_offset(256, 32) == 144
     assert oracle.payload_bytes(1 << 24, 16) * 8 / (1 << 24) == 4.625   # bits per element
-    for bad in [(0, 16), (100, 16), (512, 8), (-256, 16)]:
+    assert oracle.payload_bytes(100, 16) == 128 + 16 + 4         # one zero-padded block
+    for bad in [(0, 16), (512, 8), (-256, 16)]:
         assert oracle.payload_bytes(*bad) == 0
 
 
@@ -465,3 +466,29 @@ def test_reduce_sums_in_the_transform_domain():
         cc = _codes(c2)
         zt = zt + (GRID[cc & 7] * np.where(cc >= 8, -1.0, 1.0)).astype(np.float32) * S2
     _check_codes_optimal(zt, q, _codes(codes), S)
+
+
+@pytest.mark.parametrize("scales,G", [("dual", 16), ("dual", 32), ("e8m0", 32)])
+@pytest.mark.parametrize("n", [1, 17, 255, 257, 256 * 3 + 1, 4096 + 100, 256 * 37 + 255])
+def test_tail_is_the_zero_padded_block(n, scales, G):
+    """n not a multiple of 256: the payload is that of the input zero-padded to whole blocks
+    (written out here by the caller, not by the oracle), and the decode gives the first n
+    values of the padded decode, leaving everything past n untouched."""
+    m = -(-n // 256) * 256
+    x = inputs.sweep(4096 * 4, seed=n % 11).ravel()[:n].copy()
+    xp = np.zeros(m, np.uint16)
+    xp[:n] = x
+    for fwht in (0, 1):
+        p = oracle.compress(x, group=G, fwht=fwht, scales=scales)
+        pp = oracle.compress(xp, group=G, fwht=fwht, scales=scales)
+        assert p.size == oracle.payload_bytes(m, G, scales)
+        assert np.array_equal(p, pp)
+        d = np.full(n + 7, 3.0, np.float32)
+        oracle.decompress_accumulate(p, n, d[:n], beta=0, group=G, fwht=fwht, scales=scales)
+        dp = np.zeros(m, np.float32)
+        oracle.decompress_accumulate(pp, m, dp, beta=0, group=G, fwht=fwht, scales=scales)
+        assert np.array_equal(d[:n], dp[:n]) and (d[n:] == 3.0).all()
+        y = oracle.roundtrip(x, group=G, fwht=fwht, scales=scales)
+        assert np.array_equal(y, oracle.roundtrip(xp, group=G, fwht=fwht, scales=scales)[:n])
+        r = oracle.reduce_requantize([p, p], n, group=G, scales=scales)
+        assert np.array_equal(r, oracle.reduce_requantize([pp, pp], m, group=G, scales=scales))
