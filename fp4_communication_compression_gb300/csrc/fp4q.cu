@@ -1152,6 +1152,133 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
   }
 }
 
+// Last partial block of a tensor whose length is not a multiple of 256 (it is zero-padded
+// to 256 elements): one warp loads it with bounds checks and runs the same per-block steps
+// as the tiled kernels. All 8 four-lane groups of the warp work on that block, so the
+// transpose and the shuffles see a full warp; only the first group stores.
+constexpr int kTailThreads = 32;
+
+// Row 4 l4 + k, pair j = elements 16 (4 l4 + k) + 2j and + 1 of the block (layout A); with
+// bfly, each pair goes through the stride-1 butterfly in FP32, as the fused BF16 load does.
+__device__ __forceinline__ void tail_load_bf16(const uint16_t* x, int len, int l4, Rows v, bool bfly) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = 16 * (4 * l4 + k) + 2 * j;
+      const float a = e < len ? __uint_as_float((uint32_t)x[e] << 16) : 0.0f;
+      const float b = e + 1 < len ? __uint_as_float((uint32_t)x[e + 1] << 16) : 0.0f;
+      v[k][j] = bfly ? make_float2(__fadd_rn(a, b), __fsub_rn(a, b)) : make_float2(a, b);
+    }
+}
+
+// dst[e] = BETA ? dst[e] + v : v for the block's elements below len (layout A rows).
+template <int DT, int BETA>
+__device__ __forceinline__ void tail_store(void* dst, int len, int l4, const Rows v) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = 16 * (4 * l4 + k) + 2 * j + h;
+        if (e >= len) continue;
+        const float x = h ? v[k][j].y : v[k][j].x;
+        if (DT == FP4Q_BF16) {
+          uint16_t* d = static_cast<uint16_t*>(dst);
+          const float o = BETA ? __fadd_rn(__uint_as_float((uint32_t)d[e] << 16), x) : x;
+          d[e] = (uint16_t)(f2_to_bf16x2(make_float2(o, 0.0f)) & 0xffffu);
+        } else {
+          float* d = static_cast<float*>(dst);
+          d[e] = BETA ? __fadd_rn(d[e], x) : x;
+        }
+      }
+}
+
+// Forward steps of compress / roundtrip on a loaded block; leaves the codes and scales in q
+// and the values in layout B (FWHT) or A.
+template <int G, int FWHT, bool MX>
+__device__ __forceinline__ void tail_quantize(Rows v, const XposeAddr& xa, Quant& q) {
+  if (FWHT) {
+    level1_fwd_from2(v);
+    rows_bfly(v, 1);
+    rows_bfly(v, 2);
+    transpose<true>(v, xa);
+    rows_bfly(v, 1);
+    rows_bfly(v, 2);
+    if (MX) {
+      scale_rows_16th(v);
+      quantize_mx<true>(v, q);
+    } else {
+      quantize<G, true, true>(v, q);
+    }
+  } else {
+    if (MX) quantize_mx<false>(v, q); else quantize<G, false, false>(v, q);
+  }
+}
+
+// Inverse transform of decoded values (layout B in, layout A out).
+__device__ __forceinline__ void tail_inverse(Rows v, const XposeAddr& xa) {
+  rows_bfly(v, 2);
+  rows_bfly(v, 1);
+  transpose<false>(v, xa);
+  rows_bfly(v, 2);
+  rows_bfly(v, 1);
+  level1_inv(v);
+}
+
+template <int G, int FWHT, bool MX>
+__global__ void __launch_bounds__(kTailThreads)
+tail_compress_kernel(const uint16_t* x, int len, Payload P, int64_t gb) {
+  __shared__ __align__(1024) uint8_t xbuf[kXBufBytes];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int lane = threadIdx.x, blk = lane >> 2, l4 = lane & 3;
+  const XposeAddr xa = xpose_addr(smem_addr(xbuf), blk, l4);
+  Rows v;
+  tail_load_bf16(x, len, l4, v, FWHT != 0);
+  Quant q;
+  tail_quantize<G, FWHT, MX>(v, xa, q);
+  if (blk == 0) store_block<G, FWHT != 0, MX>(P, gb, l4, q);
+}
+
+template <int G, int FWHT, int DT, int BETA, bool MX>
+__global__ void __launch_bounds__(kTailThreads)
+tail_decompress_kernel(Payload P, int64_t gb, void* dst, int len, float negzero) {
+  __shared__ __align__(1024) uint8_t xbuf[kXBufBytes];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int lane = threadIdx.x, blk = lane >> 2, l4 = lane & 3;
+  const XposeAddr xa = xpose_addr(smem_addr(xbuf), blk, l4);
+  PayRaw r;
+  pay_load<G, FWHT != 0, MX>(P, gb, l4, r);
+  float S[4];
+  pay_scales<G, FWHT != 0, MX>(r, l4, S);
+  if (FWHT) scale_by_16th(S);
+  Rows v;
+  dequantize(r.code, S, v, negzero);
+  if (FWHT) tail_inverse(v, xa);
+  if (blk == 0) tail_store<DT, BETA>(dst, len, l4, v);
+}
+
+template <int G, int FWHT, bool MX>
+__global__ void __launch_bounds__(kTailThreads)
+tail_roundtrip_kernel(const uint16_t* x, void* y, int len, float negzero) {
+  __shared__ __align__(1024) uint8_t xbuf[kXBufBytes];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int lane = threadIdx.x, blk = lane >> 2, l4 = lane & 3;
+  const XposeAddr xa = xpose_addr(smem_addr(xbuf), blk, l4);
+  Rows v;
+  tail_load_bf16(x, len, l4, v, FWHT != 0);
+  Quant q;
+  tail_quantize<G, FWHT, MX>(v, xa, q);
+  if (FWHT) scale_by_16th(q.S);
+  dequantize(q.code, q.S, v, negzero);
+  if (FWHT) tail_inverse(v, xa);
+  if (blk == 0) tail_store<FP4Q_BF16, 0>(y, len, l4, v);
+}
+
 // Self-test of the bounded wait: one warp waits on a barrier phase that nothing completes;
 // the wait gives up after `polls` polls and records kFaultSelftest.
 __global__ void selftest_wait_kernel(uint32_t polls) {
@@ -1299,7 +1426,10 @@ fp4q_status check_params(const fp4q_params* p, int& G, int& fwht, bool& mx) {
 }
 
 // The kernels address tiles with 32-bit TMA line coordinates: n < 2^37 keeps them in range.
-bool size_ok(int64_t n) { return n > 0 && n % FP4Q_BLOCK == 0 && n < ((int64_t)1 << 37); }
+bool size_ok(int64_t n) { return n > 0 && n < ((int64_t)1 << 37); }
+
+// Elements the payload covers: n rounded up to whole blocks (the last one zero-padded).
+int64_t padded_n(int64_t n) { return (n + FP4Q_BLOCK - 1) / FP4Q_BLOCK * FP4Q_BLOCK; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -1314,49 +1444,82 @@ TileLoop tiles_of(int64_t n) {
   return T;
 }
 
+// Tail launch: one warp for the last partial block.
+template <class K, class... Args>
+fp4q_status launch_tail(K kernel, cudaStream_t s, Args&&... args) {
+  Launch L;
+  L.grid = 1;
+  L.smem = 0;
+  return launch_pdl(kernel, L, kTailThreads, s, std::forward<Args>(args)...);
+}
+
+// Full blocks through the tiled kernel, then the zero-padded last block (if any) through
+// the one-warp tail kernel; the payload layout is that of the padded length.
 template <int G, int F, bool MX>
 fp4q_status launch_compress(const void* x, int64_t n, void* payload, cudaStream_t s) {
-  TileLoop T = tiles_of(n);
-  CUtensorMap xm;
-  if (!line_map(&xm, x, n, false)) return FP4Q_ERR_CUDA;
-  auto k = compress_kernel<G, F, MX>;
-  Launch L;
-  fp4q_status st = plan(k, kCompressWarps, WarpSmemLayout<kCompressWarps, kCompressStages, 4096>::kCtaBytes,
-                        T.tiles, L);
-  if (st != FP4Q_OK) return st;
-  return launch_pdl(k, L, kCompressWarps * 32, s, xm, payload_of(payload, n, G, MX), T);
+  const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
+  const Payload P = payload_of(payload, padded_n(n), G, MX);
+  if (nfull > 0) {
+    TileLoop T = tiles_of(nfull);
+    CUtensorMap xm;
+    if (!line_map(&xm, x, nfull, false)) return FP4Q_ERR_CUDA;
+    auto k = compress_kernel<G, F, MX>;
+    Launch L;
+    fp4q_status st = plan(k, kCompressWarps, WarpSmemLayout<kCompressWarps, kCompressStages, 4096>::kCtaBytes,
+                          T.tiles, L);
+    if (st == FP4Q_OK) st = launch_pdl(k, L, kCompressWarps * 32, s, xm, P, T);
+    if (st != FP4Q_OK) return st;
+  }
+  if (n == nfull) return FP4Q_OK;
+  return launch_tail(tail_compress_kernel<G, F, MX>, s, static_cast<const uint16_t*>(x) + nfull,
+                     (int)(n - nfull), P, (int64_t)(nfull / FP4Q_BLOCK));
 }
 
 template <int G, int F, int DT, int B, bool MX>
 fp4q_status launch_decompress(const void* payload, int64_t n, void* dst, cudaStream_t s) {
-  TileLoop T = tiles_of(n);
-  CUtensorMap dm;
-  if (!line_map(&dm, dst, n, DT == FP4Q_F32)) return FP4Q_ERR_CUDA;
-  auto k = decompress_kernel<G, F, DT, B, MX>;
-  constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
-  Launch L;
-  fp4q_status st = plan(k, kDecompressWarps,
-                        WarpSmemLayout<kDecompressWarps, kDecompressStages, B ? TB : 0>::kCtaBytes, T.tiles, L,
-                        kDecompressGridCtas);
-  if (st != FP4Q_OK) return st;
-  return launch_pdl(k, L, kDecompressWarps * 32, s, dm, payload_of(const_cast<void*>(payload), n, G, MX), T);
+  const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
+  const Payload P = payload_of(const_cast<void*>(payload), padded_n(n), G, MX);
+  if (nfull > 0) {
+    TileLoop T = tiles_of(nfull);
+    CUtensorMap dm;
+    if (!line_map(&dm, dst, nfull, DT == FP4Q_F32)) return FP4Q_ERR_CUDA;
+    auto k = decompress_kernel<G, F, DT, B, MX>;
+    constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
+    Launch L;
+    fp4q_status st = plan(k, kDecompressWarps,
+                          WarpSmemLayout<kDecompressWarps, kDecompressStages, B ? TB : 0>::kCtaBytes, T.tiles, L,
+                          kDecompressGridCtas);
+    if (st == FP4Q_OK) st = launch_pdl(k, L, kDecompressWarps * 32, s, dm, P, T);
+    if (st != FP4Q_OK) return st;
+  }
+  if (n == nfull) return FP4Q_OK;
+  void* dtail = static_cast<uint8_t*>(dst) + nfull * (DT == FP4Q_BF16 ? 2 : 4);
+  return launch_tail(tail_decompress_kernel<G, F, DT, B, MX>, s, P, (int64_t)(nfull / FP4Q_BLOCK), dtail,
+                     (int)(n - nfull), -0.0f);
 }
 
 template <int G, int F, bool MX>
 fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) {
-  TileLoop T = tiles_of(n);
-  CUtensorMap xm, ym;
-  if (!line_map(&xm, x, n, false) || !line_map(&ym, y, n, false)) return FP4Q_ERR_CUDA;
-  auto k = roundtrip_kernel<G, F, MX>;
-  Launch L;
-  fp4q_status st = plan(k, kRoundtripWarps, WarpSmemLayout<kRoundtripWarps, kRoundtripStages, 4096>::kCtaBytes,
-                        T.tiles, L);
-  if (st != FP4Q_OK) return st;
-  return launch_pdl(k, L, kRoundtripWarps * 32, s, xm, ym, T);
+  const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
+  if (nfull > 0) {
+    TileLoop T = tiles_of(nfull);
+    CUtensorMap xm, ym;
+    if (!line_map(&xm, x, nfull, false) || !line_map(&ym, y, nfull, false)) return FP4Q_ERR_CUDA;
+    auto k = roundtrip_kernel<G, F, MX>;
+    Launch L;
+    fp4q_status st = plan(k, kRoundtripWarps, WarpSmemLayout<kRoundtripWarps, kRoundtripStages, 4096>::kCtaBytes,
+                          T.tiles, L);
+    if (st == FP4Q_OK) st = launch_pdl(k, L, kRoundtripWarps * 32, s, xm, ym, T);
+    if (st != FP4Q_OK) return st;
+  }
+  if (n == nfull) return FP4Q_OK;
+  return launch_tail(tail_roundtrip_kernel<G, F, MX>, s, static_cast<const uint16_t*>(x) + nfull,
+                     static_cast<void*>(static_cast<uint16_t*>(y) + nfull), (int)(n - nfull), -0.0f);
 }
 
 template <int G, int R, bool MX>
 fp4q_status launch_reduce_r(const RankPtrs& in, int64_t n, void* out, cudaStream_t s) {
+  n = padded_n(n);   // the reduce works on whole (zero-padded) blocks of the payloads
   TileLoop T = tiles_of(n);
   auto k = reduce_kernel<G, R, MX>;
   Launch L;
@@ -1370,7 +1533,7 @@ fp4q_status launch_reduce(const void* const* payloads, int R, int64_t n, void* o
   RankPtrs in;
   memset(&in, 0, sizeof(in));
   for (int r = 0; r < R; ++r) {
-    const Payload p = payload_of(const_cast<void*>(payloads[r]), n, G, MX);
+    const Payload p = payload_of(const_cast<void*>(payloads[r]), padded_n(n), G, MX);
     in.codes[r] = p.codes;
     in.gsc[r] = p.gsc;
     in.bsc[r] = p.bsc;
@@ -1388,7 +1551,8 @@ fp4q_status launch_reduce(const void* const* payloads, int R, int64_t n, void* o
 }
 
 size_t payload_bytes_of(int64_t n, int G, bool mx) {
-  return (size_t)(n / 2 + pad16(n / G) + (mx ? 0 : 4 * (n / FP4Q_BLOCK)));
+  const int64_t m = padded_n(n);
+  return (size_t)(m / 2 + pad16(m / G) + (mx ? 0 : 4 * (m / FP4Q_BLOCK)));
 }
 
 template <int G, bool MX>
@@ -1420,14 +1584,14 @@ size_t fp4q_gscale_offset(int64_t n, const fp4q_params* params) {
   int G, f;
   bool mx;
   if (!size_ok(n) || check_params(params, G, f, mx) != FP4Q_OK) return 0;
-  return (size_t)(n / 2);
+  return (size_t)(padded_n(n) / 2);
 }
 
 size_t fp4q_bscale_offset(int64_t n, const fp4q_params* params) {
   int G, f;
   bool mx;
   if (!size_ok(n) || check_params(params, G, f, mx) != FP4Q_OK) return 0;
-  return (size_t)(n / 2 + pad16(n / G));
+  return (size_t)(padded_n(n) / 2 + pad16(padded_n(n) / G));
 }
 
 fp4q_status fp4q_compress(const void* x_bf16, int64_t n, void* payload, const fp4q_params* params,
@@ -1526,7 +1690,7 @@ const char* fp4q_status_string(fp4q_status status) {
   switch (status) {
     case FP4Q_OK: return "ok";
     case FP4Q_ERR_NULL: return "null pointer";
-    case FP4Q_ERR_SIZE: return "n must be a positive multiple of 256 below 2^37";
+    case FP4Q_ERR_SIZE: return "n must be positive and below 2^37";
     case FP4Q_ERR_ALIGN: return "pointer not 16-byte aligned";
     case FP4Q_ERR_PARAM: return "invalid parameter (group, block, fwht, scales, R, dtype, beta or polls)";
     case FP4Q_ERR_OVERLAP: return "output overlaps an input";

@@ -20,7 +20,10 @@
  * this contract:
  *
  *   Block.   The tensor is cut into blocks of FP4Q_BLOCK = 256 consecutive elements.
- *            n must be a positive multiple of 256 (no tail handling).
+ *            Any n >= 1: a last partial block is zero-padded to 256 elements (+0), the
+ *            payload covers ceil(n/256) blocks, and every decode writes back only the n
+ *            elements (the pages say nothing about other lengths; this is the build's
+ *            reading).
  *   FWHT.    (fwht = 1) per block, y = (1/16) * H256 * x with H256 the Sylvester-ordered
  *            Walsh-Hadamard matrix, H256 = H16 (x) H16. It is evaluated as the butterfly
  *            sequence h = 1, 2, 4, ..., 128: for every j with (j & h) == 0,
@@ -100,7 +103,7 @@ extern "C" {
 typedef enum fp4q_status {
   FP4Q_OK = 0,
   FP4Q_ERR_NULL = 1,     /* a required pointer is NULL                                  */
-  FP4Q_ERR_SIZE = 2,     /* n <= 0, n % 256 != 0, or n >= 2^37                          */
+  FP4Q_ERR_SIZE = 2,     /* n <= 0 or n >= 2^37                                         */
   FP4Q_ERR_ALIGN = 3,    /* a data pointer is not 16-byte aligned                       */
   FP4Q_ERR_PARAM = 4,    /* bad params: group not 16/32, block not 256, fwht not 0/1,
                             scales not 0/1 or E8M0 with group != 32, R outside [1, 8],
@@ -121,8 +124,9 @@ typedef enum fp4q_dtype {
   FP4Q_F32 = 1    /* destination is float32                                             */
 } fp4q_dtype;
 
-/* Bytes of the payload for n elements: n/2 + pad16(n/G) + 4*(n/256) (dual scales) or
- * n/2 + pad16(n/32) (E8M0 scales). Returns 0 when n or params are invalid.
+/* Bytes of the payload for n elements, with m = n rounded up to a multiple of 256:
+ * m/2 + pad16(m/G) + 4*(m/256) (dual scales) or m/2 + pad16(m/32) (E8M0 scales).
+ * Returns 0 when n or params are invalid.
  * params == NULL means the defaults {16, 256, 1, FP4Q_SCALES_DUAL}. */
 size_t fp4q_payload_bytes(int64_t n, const fp4q_params* params);
 

@@ -43,7 +43,7 @@ def test_status_strings(L):
     assert _lib.status_string(99) == "unknown status"
 
 
-@pytest.mark.parametrize("n", [256, 4096, 256 * 17, 1 << 24, 256 * 1001])
+@pytest.mark.parametrize("n", [256, 4096, 256 * 17, 1 << 24, 256 * 1001, 1, 100, 4095, 256 * 1001 + 17])
 @pytest.mark.parametrize("G", [16, 32])
 def test_payload_layout_matches_oracle(L, n, G):
     p = _lib.params(G, 1)
@@ -65,8 +65,11 @@ def test_e8m0_payload_layout_matches_oracle(L, n):
 
 def test_payload_bytes_defaults_and_invalid(L):
     assert L.fp4q_payload_bytes(4096, None) == 2368
-    for n in (0, -256, 100, 1 << 37, 1 << 40):
+    for n in (0, -256, 1 << 37, 1 << 40):
         assert L.fp4q_payload_bytes(n, None) == 0
+    # a length that is not a multiple of 256 gets a zero-padded last block
+    assert L.fp4q_payload_bytes(100, None) == 128 + 16 + 4
+    assert L.fp4q_payload_bytes(4096 + 1, None) == L.fp4q_payload_bytes(4096 + 256, None)
     for g, b, f in [(8, 256, 1), (16, 128, 1), (16, 256, 2), (64, 256, 0)]:
         assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(g, b, f))) == 0
     # E8M0 scales need group 32; unknown scale formats are rejected
@@ -85,7 +88,7 @@ def test_compress_argument_errors(L):
     pp = ctypes.byref(P)
     assert L.fp4q_compress(None, 4096, B, pp, None) == _lib.ERR_NULL
     assert L.fp4q_compress(A, 4096, None, pp, None) == _lib.ERR_NULL
-    for n in (0, -256, 100, 4095, 1 << 37, 1 << 40):
+    for n in (0, -256, 1 << 37, 1 << 40):
         assert L.fp4q_compress(A, n, B, pp, None) == _lib.ERR_SIZE
     assert L.fp4q_compress(A + 8, 4096, B, pp, None) == _lib.ERR_ALIGN
     assert L.fp4q_compress(A, 4096, B + 2, pp, None) == _lib.ERR_ALIGN
@@ -103,7 +106,7 @@ def test_decompress_argument_errors(L):
     assert f(A, 4096, B, 2, 1, pp, None) == _lib.ERR_PARAM
     assert f(A, 4096, B, _lib.BF16, 2, pp, None) == _lib.ERR_PARAM
     assert f(A, 4096, B, _lib.F32, -1, pp, None) == _lib.ERR_PARAM
-    assert f(A, 300, B, _lib.BF16, 1, pp, None) == _lib.ERR_SIZE
+    assert f(A, 0, B, _lib.BF16, 1, pp, None) == _lib.ERR_SIZE
     assert f(A + 4, 4096, B, _lib.BF16, 1, pp, None) == _lib.ERR_ALIGN
     assert f(A, 4096, B + 4, _lib.F32, 0, pp, None) == _lib.ERR_ALIGN
     assert f(A, 4096, A + 2048, _lib.BF16, 1, pp, None) == _lib.ERR_OVERLAP
@@ -116,7 +119,7 @@ def test_roundtrip_argument_errors(L):
     f = L.fp4q_roundtrip
     assert f(None, 4096, B, pp, None) == _lib.ERR_NULL
     assert f(A, 4096, None, pp, None) == _lib.ERR_NULL
-    assert f(A, 257, B, pp, None) == _lib.ERR_SIZE
+    assert f(A, -1, B, pp, None) == _lib.ERR_SIZE
     assert f(A, 4096, B + 8, pp, None) == _lib.ERR_ALIGN
     assert f(A, 4096, A, pp, None) == _lib.ERR_OVERLAP
     assert f(A, 4096, A + 8176, pp, None) == _lib.ERR_OVERLAP
@@ -136,7 +139,7 @@ def test_reduce_argument_errors(L):
     assert f(None, 2, 4096, B, pp, None) == _lib.ERR_NULL
     assert f(two, 2, 4096, None, pp, None) == _lib.ERR_NULL
     assert f(arr(A, None), 2, 4096, B, pp, None) == _lib.ERR_NULL
-    assert f(two, 2, 1000, B, pp, None) == _lib.ERR_SIZE
+    assert f(two, 2, 0, B, pp, None) == _lib.ERR_SIZE
     assert f(arr(A, A + 0x10008), 2, 4096, B, pp, None) == _lib.ERR_ALIGN
     assert f(two, 2, 4096, B + 4, pp, None) == _lib.ERR_ALIGN
     assert f(two, 2, 4096, A + 0x10000 + 1024, pp, None) == _lib.ERR_OVERLAP
