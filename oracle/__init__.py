@@ -64,6 +64,8 @@ def _load():
             "oracle_compress": (I, [P, I64, P, I, I, I, P]),
             "oracle_decompress_accumulate": (I, [P, I64, P, I, I, I, I, I]),
             "oracle_roundtrip": (I, [P, I64, P, I, I, I]),
+            "oracle_compress_f32": (I, [P, I64, P, I, I, I, P]),
+            "oracle_roundtrip_f32": (I, [P, I64, P, I, I, I]),
             "oracle_reduce_requantize": (I, [P, I, I64, P, I, I, P]),
             "oracle_e4m3_encode_array": (None, [P, P, I64]),
             "oracle_e2m1_encode_array": (None, [P, P, I64]),
@@ -200,6 +202,34 @@ def compress(x_bf16: np.ndarray, group: int | None = None, fwht: int = 1, want_q
     if rc != 0:
         raise ValueError(f"oracle_compress failed ({rc})")
     return (out, q) if want_q else out
+
+
+def compress_f32(x: np.ndarray, group: int | None = None, fwht: int = 1, want_q: bool = False,
+                 scales: str = "dual"):
+    """FP32 input (used as it is): returns the payload (uint8) and, if want_q, every q."""
+    G, mx = _fmt(group, scales)
+    x = _c(x, np.float32).ravel()
+    n = x.size
+    nbytes = payload_bytes(n, G, scales)
+    if nbytes == 0:
+        raise ValueError(f"invalid n={n} or group={G} for scales={scales}")
+    out = np.zeros(nbytes, np.uint8)
+    q = np.empty(n, np.float32) if want_q else None
+    rc = _load().oracle_compress_f32(_ptr(x), n, _ptr(out), G, fwht, mx, _ptr(q) if want_q else None)
+    if rc != 0:
+        raise ValueError(f"oracle_compress_f32 failed ({rc})")
+    return (out, q) if want_q else out
+
+
+def roundtrip_f32(x: np.ndarray, group: int | None = None, fwht: int = 1, scales: str = "dual") -> np.ndarray:
+    """FP32 in, FP32 out: decode(compress_f32(x)) without a BF16 rounding of the result."""
+    G, mx = _fmt(group, scales)
+    x = _c(x, np.float32).ravel()
+    y = np.empty_like(x)
+    rc = _load().oracle_roundtrip_f32(_ptr(x), x.size, _ptr(y), G, fwht, mx)
+    if rc != 0:
+        raise ValueError(f"oracle_roundtrip_f32 failed ({rc})")
+    return y
 
 
 def decompress_accumulate(payload: np.ndarray, n: int, dst: np.ndarray, beta: int,

@@ -318,12 +318,12 @@ void oracle_set_threads(int t) {
 #endif
 }
 
-/* Compress: per block, widen BF16 to FP32, FWHT (if fwht), quantise, pack.
- * Returns 0, or -1 on invalid arguments. q_out (optional) receives the pre-rounding q of
- * every element. */
-int oracle_compress(const uint16_t* x, int64_t n, uint8_t* payload, int G, int fwht, int mx,
-                    float* q_out) {
-  if (!valid(n, G, mx) || (fwht != 0 && fwht != 1) || !x || !payload) return -1;
+/* Compress of BF16 (x16) or FP32 (x32) input, exactly one of them non-NULL: per block,
+ * widen (BF16) or take (FP32) the values, FWHT (if fwht), quantise, pack. Returns 0, or -1
+ * on invalid arguments. q_out (optional) receives the pre-rounding q of every element. */
+static int compress_any(const uint16_t* x16, const float* x32, int64_t n, uint8_t* payload, int G, int fwht,
+                        int mx, float* q_out) {
+  if (!valid(n, G, mx) || (fwht != 0 && fwht != 1) || (!x16 && !x32) || !payload) return -1;
   const int64_t m = padded(n), nb = m / ORACLE_BLOCK;
   uint8_t* codes = payload;
   uint8_t* gsc = payload + oracle_gscale_offset(n, G, mx);
@@ -336,7 +336,7 @@ int oracle_compress(const uint16_t* x, int64_t n, uint8_t* payload, int G, int f
     float s_b;
     for (int i = 0; i < ORACLE_BLOCK; ++i) {
       const int64_t e = b * ORACLE_BLOCK + i;
-      y[i] = e < n ? oracle_bf16_to_f32(x[e]) : 0.0f;
+      y[i] = e >= n ? 0.0f : x16 ? oracle_bf16_to_f32(x16[e]) : x32[e];
     }
     if (fwht) oracle_fwht256(y);
     float qb[ORACLE_BLOCK];
@@ -351,6 +351,20 @@ int oracle_compress(const uint16_t* x, int64_t n, uint8_t* payload, int G, int f
     pack_block(code, codes + b * (ORACLE_BLOCK / 2));
   }
   return 0;
+}
+
+/* Compress: per block, widen BF16 to FP32, FWHT (if fwht), quantise, pack. */
+int oracle_compress(const uint16_t* x, int64_t n, uint8_t* payload, int G, int fwht, int mx,
+                    float* q_out) {
+  if (!x) return -1;
+  return compress_any(x, NULL, n, payload, G, fwht, mx, q_out);
+}
+
+/* Compress of FP32 input: the same steps with the input used as it is (no widening). */
+int oracle_compress_f32(const float* x, int64_t n, uint8_t* payload, int G, int fwht, int mx,
+                        float* q_out) {
+  if (!x) return -1;
+  return compress_any(NULL, x, n, payload, G, fwht, mx, q_out);
 }
 
 /* Decode block b of a payload to 256 FP32 values: x~ = grid(code) * S, then the inverse
@@ -406,6 +420,18 @@ int oracle_roundtrip(const uint16_t* x, int64_t n, uint16_t* y, int G, int fwht,
   if (!p) return -2;
   int rc = oracle_compress(x, n, p, G, fwht, mx, NULL);
   if (rc == 0) rc = oracle_decompress_accumulate(p, n, y, 0, 0, G, fwht, mx);
+  free(p);
+  return rc;
+}
+
+/* FP32 roundtrip: y = decode(compress_f32(x)) in FP32 (no BF16 rounding of the output). */
+int oracle_roundtrip_f32(const float* x, int64_t n, float* y, int G, int fwht, int mx) {
+  int64_t bytes = oracle_payload_bytes(n, G, mx);
+  if (bytes == 0 || !x || !y) return -1;
+  uint8_t* p = (uint8_t*)malloc((size_t)bytes);
+  if (!p) return -2;
+  int rc = oracle_compress_f32(x, n, p, G, fwht, mx, NULL);
+  if (rc == 0) rc = oracle_decompress_accumulate(p, n, y, 1, 0, G, fwht, mx);
   free(p);
   return rc;
 }

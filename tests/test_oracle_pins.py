@@ -492,3 +492,39 @@ def test_tail_is_the_zero_padded_block(n, scales, G):
         assert np.array_equal(y, oracle.roundtrip(xp, group=G, fwht=fwht, scales=scales)[:n])
         r = oracle.reduce_requantize([p, p], n, group=G, scales=scales)
         assert np.array_equal(r, oracle.reduce_requantize([pp, pp], m, group=G, scales=scales))
+
+
+@pytest.mark.parametrize("scales,G", [("dual", 16), ("dual", 32), ("e8m0", 32)])
+def test_f32_input_equals_bf16_input_on_bf16_values(scales, G):
+    """FP32 input holding bfloat16-exact values must give the payload of the BF16 path (the
+    widening is the only difference), at a length with a partial last block."""
+    x = inputs.sweep(4096 * 8, seed=4).ravel()[:4096 * 8 - 77].copy()
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float32)
+    for fwht in (0, 1):
+        p16 = oracle.compress(x, group=G, fwht=fwht, scales=scales)
+        p32 = oracle.compress_f32(xf, group=G, fwht=fwht, scales=scales)
+        assert np.array_equal(p16, p32)
+        y32 = oracle.roundtrip_f32(xf, group=G, fwht=fwht, scales=scales)
+        d = np.zeros(xf.size, np.float32)
+        oracle.decompress_accumulate(p32, xf.size, d, beta=0, group=G, fwht=fwht, scales=scales)
+        assert np.array_equal(y32.view(np.uint32), d.view(np.uint32))
+        assert np.array_equal(oracle.bf16_round(y32), oracle.roundtrip(x, group=G, fwht=fwht, scales=scales))
+
+
+def test_f32_input_codes_are_optimal():
+    """General FP32 input (not BF16-representable): with the FWHT off every code is the
+    nearest grid point of q, which is y times the group's reciprocal scale, and the
+    low mantissa bits of the input reach the codes (they differ from the BF16-rounded input's)."""
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal(256 * 64) * np.exp(rng.uniform(-3, 3, 64).repeat(256))).astype(np.float32)
+    p, q = oracle.compress_f32(x, fwht=0, want_q=True)
+    codes, _, _ = oracle.split_payload(p, x.size)
+    c = np.empty(x.size, np.uint8)
+    c[0::2], c[1::2] = codes & 15, codes >> 4
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    dist = np.abs(np.abs(q.astype(np.float64))[:, None] - grid[None, :])
+    best = dist.min(axis=1)
+    assert np.all(dist[np.arange(x.size), c & 7] == best)
+    assert np.all((c >> 3) == np.signbit(q))
+    pb = oracle.compress(inputs.to_bf16_bits(x), fwht=0)
+    assert not np.array_equal(p, pb)
