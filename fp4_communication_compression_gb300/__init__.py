@@ -5,7 +5,7 @@ function takes CUDA tensors, runs on the current torch stream (or the ``stream``
 and returns without synchronising. The codec itself runs only in the sm_103a kernels of
 ``csrc/fp4q.cu``; there is no CPU fallback (a missing library raises ``RuntimeError``).
 
-    payload = compress(x)                                  # x: bfloat16, numel % 256 == 0
+    payload = compress(x)                                  # x: bfloat16 or float32, any numel
     decompress_accumulate(payload, x.numel(), dst, beta=1) # dst += decode(payload)
     y = roundtrip(x)                                       # fused fake-quantisation
     out = reduce_requantize([p0, p1, p2, p3], n)           # emulated 4-rank reduce
@@ -66,20 +66,23 @@ def bscale_offset(n: int, group: int | None = None, fwht: int = 1, scales: str =
 
 
 def compress(x, payload=None, group: int | None = None, fwht: int = 1, stream=None, scales: str = "dual"):
-    """bfloat16 CUDA tensor -> uint8 payload tensor (allocated by torch if not given)."""
+    """bfloat16 or float32 CUDA tensor -> uint8 payload tensor (allocated by torch if not given)."""
     import torch
-    if x.dtype != torch.bfloat16:
-        raise TypeError("x must be bfloat16")
+    if x.dtype == torch.bfloat16:
+        fn, name = _lib.lib().fp4q_compress, "fp4q_compress"
+    elif x.dtype == torch.float32:
+        fn, name = _lib.lib().fp4q_compress_f32, "fp4q_compress_f32"
+    else:
+        raise TypeError("x must be bfloat16 or float32")
     n = x.numel()
     if payload is None:
         nb = payload_bytes(n, group, fwht, scales)
         if nb == 0:
-            raise ValueError(f"invalid size {n} (must be a positive multiple of 256)")
+            raise ValueError(f"invalid size {n} or parameters")
         payload = torch.empty(nb, dtype=torch.uint8, device=x.device)
     p = _lib.params(group, fwht, scales=scales)
-    st = _lib.lib().fp4q_compress(_dev(x, "x"), n, _dev(payload, "payload"), ctypes.byref(p),
-                                  _stream(stream, x.device))
-    _lib.check("fp4q_compress", st)
+    st = fn(_dev(x, "x"), n, _dev(payload, "payload"), ctypes.byref(p), _stream(stream, x.device))
+    _lib.check(name, st)
     return payload
 
 
@@ -104,16 +107,22 @@ def decompress_accumulate(payload, n: int, dst, beta: int = 1, group: int | None
 
 
 def roundtrip(x, y=None, group: int | None = None, fwht: int = 1, stream=None, scales: str = "dual"):
-    """y = bf16(decode(compress(x))) in one kernel, no payload written."""
+    """y = decode(compress(x)) in one kernel, no payload written; bfloat16 in and out, or
+    float32 in and out (no bfloat16 rounding)."""
     import torch
-    if x.dtype != torch.bfloat16:
-        raise TypeError("x must be bfloat16")
+    if x.dtype == torch.bfloat16:
+        fn, name = _lib.lib().fp4q_roundtrip, "fp4q_roundtrip"
+    elif x.dtype == torch.float32:
+        fn, name = _lib.lib().fp4q_roundtrip_f32, "fp4q_roundtrip_f32"
+    else:
+        raise TypeError("x must be bfloat16 or float32")
     if y is None:
         y = torch.empty_like(x)
+    if y.dtype != x.dtype or y.numel() != x.numel():
+        raise ValueError("y must match x in dtype and size")
     p = _lib.params(group, fwht, scales=scales)
-    st = _lib.lib().fp4q_roundtrip(_dev(x, "x"), x.numel(), _dev(y, "y"), ctypes.byref(p),
-                                   _stream(stream, x.device))
-    _lib.check("fp4q_roundtrip", st)
+    st = fn(_dev(x, "x"), x.numel(), _dev(y, "y"), ctypes.byref(p), _stream(stream, x.device))
+    _lib.check(name, st)
     return y
 
 

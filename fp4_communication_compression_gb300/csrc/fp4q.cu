@@ -809,6 +809,11 @@ __device__ __forceinline__ void tile_read_bf16_bfly(uint32_t buf, int blk, int a
     v[k][j + 3] = bf16x2_bfly(t.w);
   }
 }
+// The input tile of compress / roundtrip: BF16 (stride-1 butterfly fused into the widening
+// when BFLY) or FP32 (the same butterfly applied to each pair in FP32).
+template <bool XF, bool BFLY>
+__device__ __forceinline__ void tile_read_in(uint32_t buf, int blk, int a, Rows v);
+
 __device__ __forceinline__ void tile_write_bf16(uint32_t buf, int blk, int a, const Rows v) {
   const int line = 4 * blk + a;
   const uint32_t base = buf + (uint32_t)line * 128u, sw = (uint32_t)(line & 7);
@@ -849,6 +854,25 @@ __device__ __forceinline__ void tile_write_f32(uint32_t buf, int blk, int a, con
   }
 }
 
+__device__ __forceinline__ void pair_bfly(Rows v) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[k][j] = make_float2(__fadd_rn(v[k][j].x, v[k][j].y), __fsub_rn(v[k][j].x, v[k][j].y));
+}
+
+template <bool XF, bool BFLY>
+__device__ __forceinline__ void tile_read_in(uint32_t buf, int blk, int a, Rows v) {
+  if (XF) {
+    tile_read_f32(buf, blk, a, v);
+    if (BFLY) pair_bfly(v);
+  } else if (BFLY) {
+    tile_read_bf16_bfly(buf, blk, a, v);
+  } else {
+    tile_read_bf16(buf, blk, a, v);
+  }
+}
+
 // ------------------------------------------------------------------ kernels
 
 struct TileLoop {
@@ -881,27 +905,29 @@ __device__ __forceinline__ void staging_store(const CUtensorMap* map, int lines,
 }
 
 // K1: compress. x (bfloat16, n) -> payload. Input tiles arrive by TMA.
-template <int G, int FWHT, bool MX>
+// XF: FP32 input (8 KiB tiles of 64 lines) instead of BF16 (4 KiB, 32 lines).
+template <int G, int FWHT, bool MX, bool XF>
 __global__ void __launch_bounds__(kCompressWarps * 32, kCompressCtas)
 compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T) {
+  constexpr int IN = XF ? 8192 : 4096, LINES = XF ? kTileLinesF32 : kTileLinesBF16;
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  const WarpSmem ws = warp_smem<kCompressStages, 4096>(smem_raw, warp);
+  const WarpSmem ws = warp_smem<kCompressStages, IN>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
-    mbar_expect_tx(bar, 4096);
-    tma_load_2d(buf, &xmap, 0, (int32_t)(t * kTileLinesBF16), bar);
+    mbar_expect_tx(bar, IN);
+    tma_load_2d(buf, &xmap, 0, (int32_t)(t * LINES), bar);
   };
-  InPipe<kCompressStages, 4096> pipe{};
+  InPipe<kCompressStages, IN> pipe{};
   pipe.start(ws.stage0, ws.bar0, warp_global<kCompressWarps>(), warp_count<kCompressWarps>(), T.tiles, lane, issue);
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     const int64_t gb = t * kTileBlocks + blk;
     const bool valid = gb < T.nb;
     if (!pipe.wait()) return;
     Rows v;
-    if (FWHT) tile_read_bf16_bfly(pipe.cur(), blk, l4, v); else tile_read_bf16(pipe.cur(), blk, l4, v);
+    tile_read_in<XF, FWHT != 0>(pipe.cur(), blk, l4, v);
     pipe.refill(lane, issue);
     Quant q;
     if (FWHT) {
@@ -991,26 +1017,28 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
 }
 
 // K3: fused roundtrip. x (bfloat16) -> y = bf16(decode(compress(x))), no payload.
-template <int G, int FWHT, bool MX>
+// XF: FP32 input and output instead of BF16.
+template <int G, int FWHT, bool MX, bool XF>
 __global__ void __launch_bounds__(kRoundtripWarps * 32, kRoundtripCtas)
 roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap, TileLoop T) {
+  constexpr int IN = XF ? 8192 : 4096, LINES = XF ? kTileLinesF32 : kTileLinesBF16;
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  const WarpSmem ws = warp_smem<kRoundtripStages, 4096>(smem_raw, warp);
+  const WarpSmem ws = warp_smem<kRoundtripStages, IN>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
-    mbar_expect_tx(bar, 4096);
-    tma_load_2d(buf, &xmap, 0, (int32_t)(t * kTileLinesBF16), bar);
+    mbar_expect_tx(bar, IN);
+    tma_load_2d(buf, &xmap, 0, (int32_t)(t * LINES), bar);
   };
-  InPipe<kRoundtripStages, 4096> pipe{};
+  InPipe<kRoundtripStages, IN> pipe{};
   pipe.start(ws.stage0, ws.bar0, warp_global<kRoundtripWarps>(), warp_count<kRoundtripWarps>(), T.tiles, lane,
              issue);
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     if (!pipe.wait()) break;
     Rows v;
-    if (FWHT) tile_read_bf16_bfly(pipe.cur(), blk, l4, v); else tile_read_bf16(pipe.cur(), blk, l4, v);
+    tile_read_in<XF, FWHT != 0>(pipe.cur(), blk, l4, v);
     pipe.refill(lane, issue);
     Quant q;
     if (FWHT) {
@@ -1040,8 +1068,8 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       dequantize(q.code, q.S, v, T.negzero);
       staging_free(lane);
     }
-    tile_write_bf16(ws.xbuf, blk, l4, v);
-    staging_store(&ymap, kTileLinesBF16, t, ws.xbuf, lane);
+    if (XF) tile_write_f32(ws.xbuf, blk, l4, v); else tile_write_bf16(ws.xbuf, blk, l4, v);
+    staging_store(&ymap, LINES, t, ws.xbuf, lane);
   }
   if (lane == 0) bulk_wait_all();
 }
@@ -1160,14 +1188,19 @@ constexpr int kTailThreads = 32;
 
 // Row 4 l4 + k, pair j = elements 16 (4 l4 + k) + 2j and + 1 of the block (layout A); with
 // bfly, each pair goes through the stride-1 butterfly in FP32, as the fused BF16 load does.
-__device__ __forceinline__ void tail_load_bf16(const uint16_t* x, int len, int l4, Rows v, bool bfly) {
+template <bool XF>
+__device__ __forceinline__ float tail_elem(const void* x, int e) {
+  return XF ? static_cast<const float*>(x)[e] : __uint_as_float((uint32_t)static_cast<const uint16_t*>(x)[e] << 16);
+}
+template <bool XF>
+__device__ __forceinline__ void tail_load(const void* x, int len, int l4, Rows v, bool bfly) {
 #pragma unroll
   for (int k = 0; k < 4; ++k)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int e = 16 * (4 * l4 + k) + 2 * j;
-      const float a = e < len ? __uint_as_float((uint32_t)x[e] << 16) : 0.0f;
-      const float b = e + 1 < len ? __uint_as_float((uint32_t)x[e + 1] << 16) : 0.0f;
+      const float a = e < len ? tail_elem<XF>(x, e) : 0.0f;
+      const float b = e + 1 < len ? tail_elem<XF>(x, e + 1) : 0.0f;
       v[k][j] = bfly ? make_float2(__fadd_rn(a, b), __fsub_rn(a, b)) : make_float2(a, b);
     }
 }
@@ -1227,16 +1260,16 @@ __device__ __forceinline__ void tail_inverse(Rows v, const XposeAddr& xa) {
   level1_inv(v);
 }
 
-template <int G, int FWHT, bool MX>
+template <int G, int FWHT, bool MX, bool XF>
 __global__ void __launch_bounds__(kTailThreads)
-tail_compress_kernel(const uint16_t* x, int len, Payload P, int64_t gb) {
+tail_compress_kernel(const void* x, int len, Payload P, int64_t gb) {
   __shared__ __align__(1024) uint8_t xbuf[kXBufBytes];
   grid_dependency_wait();
   grid_launch_dependents();
   const int lane = threadIdx.x, blk = lane >> 2, l4 = lane & 3;
   const XposeAddr xa = xpose_addr(smem_addr(xbuf), blk, l4);
   Rows v;
-  tail_load_bf16(x, len, l4, v, FWHT != 0);
+  tail_load<XF>(x, len, l4, v, FWHT != 0);
   Quant q;
   tail_quantize<G, FWHT, MX>(v, xa, q);
   if (blk == 0) store_block<G, FWHT != 0, MX>(P, gb, l4, q);
@@ -1261,22 +1294,22 @@ tail_decompress_kernel(Payload P, int64_t gb, void* dst, int len, float negzero)
   if (blk == 0) tail_store<DT, BETA>(dst, len, l4, v);
 }
 
-template <int G, int FWHT, bool MX>
+template <int G, int FWHT, bool MX, bool XF>
 __global__ void __launch_bounds__(kTailThreads)
-tail_roundtrip_kernel(const uint16_t* x, void* y, int len, float negzero) {
+tail_roundtrip_kernel(const void* x, void* y, int len, float negzero) {
   __shared__ __align__(1024) uint8_t xbuf[kXBufBytes];
   grid_dependency_wait();
   grid_launch_dependents();
   const int lane = threadIdx.x, blk = lane >> 2, l4 = lane & 3;
   const XposeAddr xa = xpose_addr(smem_addr(xbuf), blk, l4);
   Rows v;
-  tail_load_bf16(x, len, l4, v, FWHT != 0);
+  tail_load<XF>(x, len, l4, v, FWHT != 0);
   Quant q;
   tail_quantize<G, FWHT, MX>(v, xa, q);
   if (FWHT) scale_by_16th(q.S);
   dequantize(q.code, q.S, v, negzero);
   if (FWHT) tail_inverse(v, xa);
-  if (blk == 0) tail_store<FP4Q_BF16, 0>(y, len, l4, v);
+  if (blk == 0) tail_store<XF ? FP4Q_F32 : FP4Q_BF16, 0>(y, len, l4, v);
 }
 
 // Self-test of the bounded wait: one warp waits on a barrier phase that nothing completes;
@@ -1455,24 +1488,24 @@ fp4q_status launch_tail(K kernel, cudaStream_t s, Args&&... args) {
 
 // Full blocks through the tiled kernel, then the zero-padded last block (if any) through
 // the one-warp tail kernel; the payload layout is that of the padded length.
-template <int G, int F, bool MX>
+template <int G, int F, bool MX, bool XF>
 fp4q_status launch_compress(const void* x, int64_t n, void* payload, cudaStream_t s) {
   const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
   const Payload P = payload_of(payload, padded_n(n), G, MX);
   if (nfull > 0) {
     TileLoop T = tiles_of(nfull);
     CUtensorMap xm;
-    if (!line_map(&xm, x, nfull, false)) return FP4Q_ERR_CUDA;
-    auto k = compress_kernel<G, F, MX>;
+    if (!line_map(&xm, x, nfull, XF)) return FP4Q_ERR_CUDA;
+    auto k = compress_kernel<G, F, MX, XF>;
     Launch L;
-    fp4q_status st = plan(k, kCompressWarps, WarpSmemLayout<kCompressWarps, kCompressStages, 4096>::kCtaBytes,
-                          T.tiles, L);
+    fp4q_status st = plan(k, kCompressWarps,
+                          WarpSmemLayout<kCompressWarps, kCompressStages, XF ? 8192 : 4096>::kCtaBytes, T.tiles, L);
     if (st == FP4Q_OK) st = launch_pdl(k, L, kCompressWarps * 32, s, xm, P, T);
     if (st != FP4Q_OK) return st;
   }
   if (n == nfull) return FP4Q_OK;
-  return launch_tail(tail_compress_kernel<G, F, MX>, s, static_cast<const uint16_t*>(x) + nfull,
-                     (int)(n - nfull), P, (int64_t)(nfull / FP4Q_BLOCK));
+  const void* xt = static_cast<const uint8_t*>(x) + nfull * (XF ? 4 : 2);
+  return launch_tail(tail_compress_kernel<G, F, MX, XF>, s, xt, (int)(n - nfull), P, (int64_t)(nfull / FP4Q_BLOCK));
 }
 
 template <int G, int F, int DT, int B, bool MX>
@@ -1498,23 +1531,25 @@ fp4q_status launch_decompress(const void* payload, int64_t n, void* dst, cudaStr
                      (int)(n - nfull), -0.0f);
 }
 
-template <int G, int F, bool MX>
+template <int G, int F, bool MX, bool XF>
 fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) {
   const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
   if (nfull > 0) {
     TileLoop T = tiles_of(nfull);
     CUtensorMap xm, ym;
-    if (!line_map(&xm, x, nfull, false) || !line_map(&ym, y, nfull, false)) return FP4Q_ERR_CUDA;
-    auto k = roundtrip_kernel<G, F, MX>;
+    if (!line_map(&xm, x, nfull, XF) || !line_map(&ym, y, nfull, XF)) return FP4Q_ERR_CUDA;
+    auto k = roundtrip_kernel<G, F, MX, XF>;
     Launch L;
-    fp4q_status st = plan(k, kRoundtripWarps, WarpSmemLayout<kRoundtripWarps, kRoundtripStages, 4096>::kCtaBytes,
-                          T.tiles, L);
+    fp4q_status st = plan(k, kRoundtripWarps,
+                          WarpSmemLayout<kRoundtripWarps, kRoundtripStages, XF ? 8192 : 4096>::kCtaBytes, T.tiles, L);
     if (st == FP4Q_OK) st = launch_pdl(k, L, kRoundtripWarps * 32, s, xm, ym, T);
     if (st != FP4Q_OK) return st;
   }
   if (n == nfull) return FP4Q_OK;
-  return launch_tail(tail_roundtrip_kernel<G, F, MX>, s, static_cast<const uint16_t*>(x) + nfull,
-                     static_cast<void*>(static_cast<uint16_t*>(y) + nfull), (int)(n - nfull), -0.0f);
+  const size_t es = XF ? 4 : 2;
+  return launch_tail(tail_roundtrip_kernel<G, F, MX, XF>, s,
+                     static_cast<const void*>(static_cast<const uint8_t*>(x) + nfull * es),
+                     static_cast<void*>(static_cast<uint8_t*>(y) + nfull * es), (int)(n - nfull), -0.0f);
 }
 
 template <int G, int R, bool MX>
@@ -1569,6 +1604,40 @@ fp4q_status dispatch_decompress(int key, const void* payload, int64_t n, void* d
   }
 }
 
+// Argument checks and dispatch of compress / roundtrip for BF16 (XF = false) or FP32 input.
+template <bool XF>
+fp4q_status compress_entry(const void* x, int64_t n, void* payload, const fp4q_params* params, void* stream) {
+  int G, F;
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
+  if (st != FP4Q_OK) return st;
+  if (!x || !payload) return FP4Q_ERR_NULL;
+  if (!size_ok(n)) return FP4Q_ERR_SIZE;
+  if (!aligned16(x) || !aligned16(payload)) return FP4Q_ERR_ALIGN;
+  if (overlap(x, (size_t)n * (XF ? 4 : 2), payload, payload_bytes_of(n, G, MX))) return FP4Q_ERR_OVERLAP;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (MX) return F ? launch_compress<32, 1, true, XF>(x, n, payload, s) : launch_compress<32, 0, true, XF>(x, n, payload, s);
+  if (G == 16) return F ? launch_compress<16, 1, false, XF>(x, n, payload, s) : launch_compress<16, 0, false, XF>(x, n, payload, s);
+  return F ? launch_compress<32, 1, false, XF>(x, n, payload, s) : launch_compress<32, 0, false, XF>(x, n, payload, s);
+}
+
+template <bool XF>
+fp4q_status roundtrip_entry(const void* x, int64_t n, void* y, const fp4q_params* params, void* stream) {
+  int G, F;
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
+  if (st != FP4Q_OK) return st;
+  if (!x || !y) return FP4Q_ERR_NULL;
+  if (!size_ok(n)) return FP4Q_ERR_SIZE;
+  if (!aligned16(x) || !aligned16(y)) return FP4Q_ERR_ALIGN;
+  const size_t bytes = (size_t)n * (XF ? 4 : 2);
+  if (overlap(x, bytes, y, bytes)) return FP4Q_ERR_OVERLAP;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (MX) return F ? launch_roundtrip<32, 1, true, XF>(x, n, y, s) : launch_roundtrip<32, 0, true, XF>(x, n, y, s);
+  if (G == 16) return F ? launch_roundtrip<16, 1, false, XF>(x, n, y, s) : launch_roundtrip<16, 0, false, XF>(x, n, y, s);
+  return F ? launch_roundtrip<32, 1, false, XF>(x, n, y, s) : launch_roundtrip<32, 0, false, XF>(x, n, y, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -1596,18 +1665,12 @@ size_t fp4q_bscale_offset(int64_t n, const fp4q_params* params) {
 
 fp4q_status fp4q_compress(const void* x_bf16, int64_t n, void* payload, const fp4q_params* params,
                           void* stream) {
-  int G, F;
-  bool MX;
-  fp4q_status st = check_params(params, G, F, MX);
-  if (st != FP4Q_OK) return st;
-  if (!x_bf16 || !payload) return FP4Q_ERR_NULL;
-  if (!size_ok(n)) return FP4Q_ERR_SIZE;
-  if (!aligned16(x_bf16) || !aligned16(payload)) return FP4Q_ERR_ALIGN;
-  if (overlap(x_bf16, (size_t)n * 2, payload, payload_bytes_of(n, G, MX))) return FP4Q_ERR_OVERLAP;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (MX) return F ? launch_compress<32, 1, true>(x_bf16, n, payload, s) : launch_compress<32, 0, true>(x_bf16, n, payload, s);
-  if (G == 16) return F ? launch_compress<16, 1, false>(x_bf16, n, payload, s) : launch_compress<16, 0, false>(x_bf16, n, payload, s);
-  return F ? launch_compress<32, 1, false>(x_bf16, n, payload, s) : launch_compress<32, 0, false>(x_bf16, n, payload, s);
+  return compress_entry<false>(x_bf16, n, payload, params, stream);
+}
+
+fp4q_status fp4q_compress_f32(const void* x_f32, int64_t n, void* payload, const fp4q_params* params,
+                              void* stream) {
+  return compress_entry<true>(x_f32, n, payload, params, stream);
 }
 
 fp4q_status fp4q_decompress_accumulate(const void* payload, int64_t n, void* dst, fp4q_dtype dtype,
@@ -1631,18 +1694,12 @@ fp4q_status fp4q_decompress_accumulate(const void* payload, int64_t n, void* dst
 
 fp4q_status fp4q_roundtrip(const void* x_bf16, int64_t n, void* y_bf16, const fp4q_params* params,
                            void* stream) {
-  int G, F;
-  bool MX;
-  fp4q_status st = check_params(params, G, F, MX);
-  if (st != FP4Q_OK) return st;
-  if (!x_bf16 || !y_bf16) return FP4Q_ERR_NULL;
-  if (!size_ok(n)) return FP4Q_ERR_SIZE;
-  if (!aligned16(x_bf16) || !aligned16(y_bf16)) return FP4Q_ERR_ALIGN;
-  if (overlap(x_bf16, (size_t)n * 2, y_bf16, (size_t)n * 2)) return FP4Q_ERR_OVERLAP;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (MX) return F ? launch_roundtrip<32, 1, true>(x_bf16, n, y_bf16, s) : launch_roundtrip<32, 0, true>(x_bf16, n, y_bf16, s);
-  if (G == 16) return F ? launch_roundtrip<16, 1, false>(x_bf16, n, y_bf16, s) : launch_roundtrip<16, 0, false>(x_bf16, n, y_bf16, s);
-  return F ? launch_roundtrip<32, 1, false>(x_bf16, n, y_bf16, s) : launch_roundtrip<32, 0, false>(x_bf16, n, y_bf16, s);
+  return roundtrip_entry<false>(x_bf16, n, y_bf16, params, stream);
+}
+
+fp4q_status fp4q_roundtrip_f32(const void* x_f32, int64_t n, void* y_f32, const fp4q_params* params,
+                               void* stream) {
+  return roundtrip_entry<true>(x_f32, n, y_f32, params, stream);
 }
 
 fp4q_status fp4q_reduce_requantize(const void* const* payloads, int32_t R, int64_t n, void* out_payload,

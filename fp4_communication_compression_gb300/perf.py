@@ -6,7 +6,7 @@
 Each kernel is timed alone with CUDA events on the launching stream, after an L2 flush
 (a write of a buffer larger than L2 followed by a read of another one), and reported as
 algorithmic GB/s (the bytes the kernel must move, G = 16; the *_mx kernels use the E8M0
-variant, group 32) and as a fraction of the measured
+variant, group 32; compress_f32 / roundtrip_f32 take FP32 input) and as a fraction of the measured
 HBM copy bandwidth in MEASURED_PEAKS.json when that file is present. Inputs are N(0,1)
 bfloat16 tensors made on the device (timing only; parity is the tests' business).
 """
@@ -37,7 +37,14 @@ ALG_BYTES = {
     "decompress_mx_bf16_b1": PAYLOAD_MX + 4,
     "roundtrip_mx": 4.0,
     "reduce_mx_r4": 5 * PAYLOAD_MX,
+    "compress_f32": 4 + PAYLOAD,
+    "roundtrip_f32": 8.0,
 }
+
+
+# the dual-scale BF16 kernels and a plain copy; the E8M0 (*_mx) and FP32-input kernels on request
+DEFAULT_KERNELS = ["compress", "decompress_bf16_b1", "decompress_bf16_b0", "decompress_f32_b1", "roundtrip",
+                   "reduce_r2", "reduce_r4", "reduce_r8", "copy_bf16"]
 
 
 def peak_gbs():
@@ -51,7 +58,7 @@ def peak_gbs():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--sizes", type=int, nargs="+", default=[1 << 24, 1 << 26, 1 << 28])
-    ap.add_argument("--kernels", nargs="+", default=[k for k in ALG_BYTES if "_mx" not in k])
+    ap.add_argument("--kernels", nargs="+", default=DEFAULT_KERNELS)
     ap.add_argument("--iters", type=int, default=30)
     args = ap.parse_args()
     dev = torch.device("cuda:0")
@@ -81,6 +88,9 @@ def main():
         y = torch.empty_like(x)
         out = torch.empty_like(ps[0])
         mx = any("_mx" in k for k in args.kernels)
+        f32 = any(k in ("compress_f32", "roundtrip_f32") for k in args.kernels)
+        xf = x.float() if f32 else None
+        yf = torch.empty_like(xf) if f32 else None
         pm = [fq.compress(x * (r + 1), scales="e8m0") for r in range(4)] if mx else None
         outm = torch.empty_like(pm[0]) if mx else None
         fns = {
@@ -97,13 +107,15 @@ def main():
             "decompress_mx_bf16_b1": lambda: fq.decompress_accumulate(pm[0], n, d16, beta=1, scales="e8m0"),
             "roundtrip_mx": lambda: fq.roundtrip(x, y=y, scales="e8m0"),
             "reduce_mx_r4": lambda: fq.reduce_requantize(pm[:4], n, out=outm, scales="e8m0"),
+            "compress_f32": lambda: fq.compress(xf, payload=ps[0]),
+            "roundtrip_f32": lambda: fq.roundtrip(xf, y=yf),
         }
         for k in args.kernels:
             t = timed(fns[k])
             gbs = ALG_BYTES[k] * n / t / 1e9
             print(json.dumps({"n": n, "kernel": k, "us": round(t * 1e6, 2), "alg_gbs": round(gbs, 1),
                               "frac_of_peak": None if not peak else round(gbs / peak, 4)}), flush=True)
-        del x, ps, d16, d32, y, out, pm, outm
+        del x, ps, d16, d32, y, out, pm, outm, xf, yf
 
 
 if __name__ == "__main__":

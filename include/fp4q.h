@@ -143,6 +143,13 @@ size_t fp4q_bscale_offset(int64_t n, const fp4q_params* params);
 fp4q_status fp4q_compress(const void* x_bf16, int64_t n, void* payload,
                           const fp4q_params* params, void* stream);
 
+/* Compress of FP32 input: x_f32 (device, n float32, 16-byte aligned) -> payload, the same
+ * steps with the input values used as they are instead of widened from BF16 (general
+ * shapes: FP32 tensors such as FP32 gradients). A BF16-exact input gives the payload
+ * fp4q_compress gives. payload must not overlap x (FP4Q_ERR_OVERLAP). */
+fp4q_status fp4q_compress_f32(const void* x_f32, int64_t n, void* payload,
+                              const fp4q_params* params, void* stream);
+
 /* Decompress-accumulate: payload (device) -> dst (device, n elements of dtype, 16-byte
  * aligned). dst = beta ? dst + x^ : x^, where x^ is the Decode step above; for a bfloat16
  * dst the sum is formed in FP32 and rounded to nearest even once. This is the receive side
@@ -159,6 +166,12 @@ fp4q_status fp4q_decompress_accumulate(const void* payload, int64_t n, void* dst
  * fp4q_decompress_accumulate(..., FP4Q_BF16, beta = 0). y must not overlap x. */
 fp4q_status fp4q_roundtrip(const void* x_bf16, int64_t n, void* y_bf16,
                            const fp4q_params* params, void* stream);
+
+/* Fused roundtrip of FP32 data: y_f32 = decode(compress_f32(x_f32)) in FP32 (no BF16
+ * rounding), bit-identical to fp4q_compress_f32 followed by
+ * fp4q_decompress_accumulate(..., FP4Q_F32, beta = 0). y must not overlap x. */
+fp4q_status fp4q_roundtrip_f32(const void* x_f32, int64_t n, void* y_f32,
+                               const fp4q_params* params, void* stream);
 
 /* Emulated R-way reduce: payloads is a HOST array of R device pointers, each a payload of
  * n elements made with the same params; out_payload (device) receives the requantized sum

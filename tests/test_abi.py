@@ -157,3 +157,16 @@ def test_fault_and_selftest_argument_errors(L):
     assert L.fp4q_fault_flags(None, 0) == _lib.ERR_NULL
     assert L.fp4q_selftest_wait_timeout(0, None) == _lib.ERR_PARAM
     assert L.fp4q_selftest_wait_timeout((1 << 20) + 1, None) == _lib.ERR_PARAM
+
+
+def test_f32_entry_points_argument_errors(L):
+    pp = ctypes.byref(P)
+    for f in (L.fp4q_compress_f32, L.fp4q_roundtrip_f32):
+        assert f(None, 4096, B, pp, None) == _lib.ERR_NULL
+        assert f(A, 0, B, pp, None) == _lib.ERR_SIZE
+        assert f(A + 4, 4096, B, pp, None) == _lib.ERR_ALIGN
+        assert f(A, 4096, B, ctypes.byref(_lib.Params(16, 256, 1, 1)), None) == _lib.ERR_PARAM
+    # FP32 input spans 4 bytes per element: an output starting inside the second half of it
+    # overlaps (it would not for a BF16 input of the same n)
+    assert L.fp4q_compress_f32(A, 4096, A + 2 * 4096 + 16, pp, None) == _lib.ERR_OVERLAP
+    assert L.fp4q_roundtrip_f32(A, 4096, A + 4 * 4096 - 16, pp, None) == _lib.ERR_OVERLAP
