@@ -50,6 +50,12 @@ def _dev(t, name):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _strided_2d(t) -> bool:
+    """A 2-D CUDA view with unit column stride and a larger row stride (a slice of a wider
+    matrix): handled by the *_2d entry points without a copy."""
+    return t.is_cuda and t.dim() == 2 and not t.is_contiguous() and t.stride(1) == 1 and t.size(0) > 1
+
+
 def payload_bytes(n: int, group: int | None = None, fwht: int = 1, scales: str = "dual") -> int:
     p = _lib.params(group, fwht, scales=scales)
     return int(_lib.lib().fp4q_payload_bytes(int(n), ctypes.byref(p)))
@@ -75,12 +81,19 @@ def compress(x, payload=None, group: int | None = None, fwht: int = 1, stream=No
     else:
         raise TypeError("x must be bfloat16 or float32")
     n = x.numel()
+    if _strided_2d(x) and x.dtype != torch.bfloat16:
+        raise ValueError("strided 2-D input must be bfloat16")
     if payload is None:
         nb = payload_bytes(n, group, fwht, scales)
         if nb == 0:
             raise ValueError(f"invalid size {n} or parameters")
         payload = torch.empty(nb, dtype=torch.uint8, device=x.device)
     p = _lib.params(group, fwht, scales=scales)
+    if _strided_2d(x):
+        st = _lib.lib().fp4q_compress_2d(ctypes.c_void_p(x.data_ptr()), x.size(0), x.size(1), x.stride(0),
+                                         _dev(payload, "payload"), ctypes.byref(p), _stream(stream, x.device))
+        _lib.check("fp4q_compress_2d", st)
+        return payload
     st = fn(_dev(x, "x"), n, _dev(payload, "payload"), ctypes.byref(p), _stream(stream, x.device))
     _lib.check(name, st)
     return payload
@@ -99,6 +112,12 @@ def decompress_accumulate(payload, n: int, dst, beta: int = 1, group: int | None
     if dst.numel() != n:
         raise ValueError("dst must have n elements")
     p = _lib.params(group, fwht, scales=scales)
+    if _strided_2d(dst):
+        st = _lib.lib().fp4q_decompress_accumulate_2d(_dev(payload, "payload"), dst.size(0), dst.size(1),
+                                                      ctypes.c_void_p(dst.data_ptr()), dst.stride(0), dt,
+                                                      int(beta), ctypes.byref(p), _stream(stream, dst.device))
+        _lib.check("fp4q_decompress_accumulate_2d", st)
+        return dst
     st = _lib.lib().fp4q_decompress_accumulate(_dev(payload, "payload"), int(n), _dev(dst, "dst"),
                                                dt, int(beta), ctypes.byref(p),
                                                _stream(stream, dst.device))
@@ -117,10 +136,18 @@ def roundtrip(x, y=None, group: int | None = None, fwht: int = 1, stream=None, s
     else:
         raise TypeError("x must be bfloat16 or float32")
     if y is None:
-        y = torch.empty_like(x)
+        y = torch.empty(x.shape, dtype=x.dtype, device=x.device)
     if y.dtype != x.dtype or y.numel() != x.numel():
         raise ValueError("y must match x in dtype and size")
     p = _lib.params(group, fwht, scales=scales)
+    if _strided_2d(x) or _strided_2d(y):
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or y.shape != x.shape:
+            raise ValueError("strided 2-D roundtrip needs bfloat16 x and y of the same 2-D shape")
+        st = _lib.lib().fp4q_roundtrip_2d(ctypes.c_void_p(x.data_ptr()), x.size(0), x.size(1), x.stride(0),
+                                          ctypes.c_void_p(y.data_ptr()), y.stride(0), ctypes.byref(p),
+                                          _stream(stream, x.device))
+        _lib.check("fp4q_roundtrip_2d", st)
+        return y
     st = fn(_dev(x, "x"), x.numel(), _dev(y, "y"), ctypes.byref(p), _stream(stream, x.device))
     _lib.check(name, st)
     return y

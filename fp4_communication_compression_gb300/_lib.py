@@ -29,6 +29,7 @@ BF16, F32 = 0, 1
 # exported symbols of the library, in the order include/fp4q.h declares them
 EXPORTS = ["fp4q_payload_bytes", "fp4q_gscale_offset", "fp4q_bscale_offset", "fp4q_compress",
            "fp4q_compress_f32", "fp4q_decompress_accumulate", "fp4q_roundtrip", "fp4q_roundtrip_f32",
+           "fp4q_compress_2d", "fp4q_decompress_accumulate_2d", "fp4q_roundtrip_2d",
            "fp4q_reduce_requantize", "fp4q_fault_flags", "fp4q_selftest_wait_timeout",
            "fp4q_status_string", "fp4q_version"]
 
@@ -86,6 +87,9 @@ def lib():
             "fp4q_compress": (ctypes.c_int, [P, I64, P, pp, P]),
             "fp4q_compress_f32": (ctypes.c_int, [P, I64, P, pp, P]),
             "fp4q_roundtrip_f32": (ctypes.c_int, [P, I64, P, pp, P]),
+            "fp4q_compress_2d": (ctypes.c_int, [P, I64, I64, I64, P, pp, P]),
+            "fp4q_decompress_accumulate_2d": (ctypes.c_int, [P, I64, I64, P, I64, ctypes.c_int, I32, pp, P]),
+            "fp4q_roundtrip_2d": (ctypes.c_int, [P, I64, I64, I64, P, I64, pp, P]),
             "fp4q_decompress_accumulate": (ctypes.c_int, [P, I64, P, ctypes.c_int, I32, pp, P]),
             "fp4q_roundtrip": (ctypes.c_int, [P, I64, P, pp, P]),
             "fp4q_reduce_requantize": (ctypes.c_int, [P, I32, I64, P, pp, P]),

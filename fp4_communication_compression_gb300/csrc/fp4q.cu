@@ -640,6 +640,18 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0,
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(src)
                : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(src)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -878,8 +890,60 @@ __device__ __forceinline__ void tile_read_in(uint32_t buf, int blk, int a, Rows 
 struct TileLoop {
   int64_t tiles;     // number of 8-block tiles
   int64_t nb;        // number of 256-element blocks
+  int64_t bpr;       // 0: the data tensor is contiguous; else blocks per row of a strided 2-D tensor
   float negzero;     // -0.0f, set by the host so the compiler cannot see its value
 };
+
+// TMA traffic of one tile of a data tensor (x, y or dst) with LPB 128-byte lines per block
+// (4 for BF16, 8 for FP32). Contiguous data is a 2-D map of lines and a tile is one box;
+// a strided 2-D tensor is a 3-D map {line, line in row, row} and a tile is one box per
+// existing block (blocks never straddle rows: cols is a multiple of 256). Each block lands
+// at the same shared-memory offset either way, so the swizzled tile layout is unchanged.
+template <int LPB>
+__device__ __forceinline__ void tile_load(const CUtensorMap* map, const TileLoop& T, int64_t t, uint32_t buf,
+                                          uint32_t bar) {
+  constexpr uint32_t BPB = 128u * LPB;
+  if (T.bpr == 0) {
+    mbar_expect_tx(bar, kTileBlocks * BPB);
+    tma_load_2d(buf, map, 0, (int32_t)(t * kTileBlocks * LPB), bar);
+    return;
+  }
+  const int64_t gb0 = t * kTileBlocks;
+  const int nv = (int)(T.nb - gb0 < kTileBlocks ? T.nb - gb0 : kTileBlocks);
+  mbar_expect_tx(bar, (uint32_t)nv * BPB);
+  int32_t row = (int32_t)(gb0 / T.bpr);
+  int32_t line = (int32_t)((gb0 - (int64_t)row * T.bpr) * LPB);
+  const int32_t row_lines = (int32_t)(T.bpr * LPB);
+  for (int b = 0; b < nv; ++b) {
+    tma_load_3d(buf + (uint32_t)b * BPB, map, 0, line, row, bar);
+    line += LPB;
+    if (line == row_lines) {
+      line = 0;
+      ++row;
+    }
+  }
+}
+template <int LPB>
+__device__ __forceinline__ void tile_store(const CUtensorMap* map, const TileLoop& T, int64_t t, uint32_t src) {
+  constexpr uint32_t BPB = 128u * LPB;
+  if (T.bpr == 0) {
+    tma_store_2d(map, 0, (int32_t)(t * kTileBlocks * LPB), src);
+    return;
+  }
+  const int64_t gb0 = t * kTileBlocks;
+  const int nv = (int)(T.nb - gb0 < kTileBlocks ? T.nb - gb0 : kTileBlocks);
+  int32_t row = (int32_t)(gb0 / T.bpr);
+  int32_t line = (int32_t)((gb0 - (int64_t)row * T.bpr) * LPB);
+  const int32_t row_lines = (int32_t)(T.bpr * LPB);
+  for (int b = 0; b < nv; ++b) {
+    tma_store_3d(map, 0, line, row, src + (uint32_t)b * BPB);
+    line += LPB;
+    if (line == row_lines) {
+      line = 0;
+      ++row;
+    }
+  }
+}
 
 template <int WARPS>
 __device__ __forceinline__ int64_t warp_global() {
@@ -894,12 +958,13 @@ __device__ __forceinline__ void staging_free(int lane) {
   __syncwarp();
 }
 // Publish the staging buffer (written with st.shared) to the TMA store of tile t.
-__device__ __forceinline__ void staging_store(const CUtensorMap* map, int lines, int64_t t, uint32_t xbuf,
+template <int LPB>
+__device__ __forceinline__ void staging_store(const CUtensorMap* map, const TileLoop& T, int64_t t, uint32_t xbuf,
                                               int lane) {
   fence_proxy_async();
   __syncwarp();
   if (lane == 0) {
-    tma_store_2d(map, 0, (int32_t)(t * lines), xbuf);
+    tile_store<LPB>(map, T, t, xbuf);
     bulk_commit();
   }
 }
@@ -909,17 +974,14 @@ __device__ __forceinline__ void staging_store(const CUtensorMap* map, int lines,
 template <int G, int FWHT, bool MX, bool XF>
 __global__ void __launch_bounds__(kCompressWarps * 32, kCompressCtas)
 compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T) {
-  constexpr int IN = XF ? 8192 : 4096, LINES = XF ? kTileLinesF32 : kTileLinesBF16;
+  constexpr int IN = XF ? 8192 : 4096;
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kCompressStages, IN>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
-  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
-    mbar_expect_tx(bar, IN);
-    tma_load_2d(buf, &xmap, 0, (int32_t)(t * LINES), bar);
-  };
+  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<XF ? 8 : 4>(&xmap, T, t, buf, bar); };
   InPipe<kCompressStages, IN> pipe{};
   pipe.start(ws.stage0, ws.bar0, warp_global<kCompressWarps>(), warp_count<kCompressWarps>(), T.tiles, lane, issue);
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
@@ -958,7 +1020,7 @@ template <int G, int FWHT, int DT, int BETA, bool MX>
 __global__ void __launch_bounds__(kDecompressWarps * 32, kDecompressCtas)
 decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop T) {
   constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
-  constexpr int LINES = DT == FP4Q_BF16 ? kTileLinesBF16 : kTileLinesF32;
+  constexpr int LPB = DT == FP4Q_BF16 ? 4 : 8;   // 128-byte lines per block of dst
   constexpr bool LB = FWHT != 0;
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
@@ -966,10 +1028,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kDecompressStages, BETA ? TB : 0>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
-  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
-    mbar_expect_tx(bar, TB);
-    tma_load_2d(buf, &dmap, 0, (int32_t)(t * LINES), bar);
-  };
+  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<LPB>(&dmap, T, t, buf, bar); };
   InPipe<kDecompressStages, TB> pipe{};
   const int64_t t0 = warp_global<kDecompressWarps>(), W = warp_count<kDecompressWarps>();
   if (BETA) pipe.start(ws.stage0, ws.bar0, t0, W, T.tiles, lane, issue);
@@ -1004,7 +1063,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
       pipe.refill(lane, issue);
     }
     if (DT == FP4Q_BF16) tile_write_bf16(ws.xbuf, blk, l4, v); else tile_write_f32(ws.xbuf, blk, l4, v);
-    staging_store(&dmap, LINES, t, ws.xbuf, lane);
+    staging_store<LPB>(&dmap, T, t, ws.xbuf, lane);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       cur.code[k][0] = nxt.code[k][0];
@@ -1021,17 +1080,14 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
 template <int G, int FWHT, bool MX, bool XF>
 __global__ void __launch_bounds__(kRoundtripWarps * 32, kRoundtripCtas)
 roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap, TileLoop T) {
-  constexpr int IN = XF ? 8192 : 4096, LINES = XF ? kTileLinesF32 : kTileLinesBF16;
+  constexpr int IN = XF ? 8192 : 4096;
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kRoundtripStages, IN>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
-  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) {
-    mbar_expect_tx(bar, IN);
-    tma_load_2d(buf, &xmap, 0, (int32_t)(t * LINES), bar);
-  };
+  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<XF ? 8 : 4>(&xmap, T, t, buf, bar); };
   InPipe<kRoundtripStages, IN> pipe{};
   pipe.start(ws.stage0, ws.bar0, warp_global<kRoundtripWarps>(), warp_count<kRoundtripWarps>(), T.tiles, lane,
              issue);
@@ -1069,7 +1125,7 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       staging_free(lane);
     }
     if (XF) tile_write_f32(ws.xbuf, blk, l4, v); else tile_write_bf16(ws.xbuf, blk, l4, v);
-    staging_store(&ymap, LINES, t, ws.xbuf, lane);
+    staging_store<XF ? 8 : 4>(&ymap, T, t, ws.xbuf, lane);
   }
   if (lane == 0) bulk_wait_all();
 }
@@ -1445,6 +1501,22 @@ bool line_map(CUtensorMap* m, const void* ptr, int64_t n, bool f32) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Strided 2-D tensor [rows, cols] with row stride ld elements, as a 3-D map of 128-byte
+// lines {line, line in row, row}; one box is one 256-element block.
+bool rows_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool f32) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t per_line = f32 ? 32 : 64, esz = f32 ? 4 : 2;
+  const cuuint64_t dims[3] = {per_line, (cuuint64_t)cols / per_line, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)ld * esz};
+  const cuuint32_t box[3] = {(cuuint32_t)per_line, f32 ? 8u : 4u, 1u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 fp4q_status check_params(const fp4q_params* p, int& G, int& fwht, bool& mx) {
   fp4q_params d = {FP4Q_GROUP_DEFAULT, FP4Q_BLOCK, 1, FP4Q_SCALES_DUAL};
   if (p) d = *p;
@@ -1473,6 +1545,7 @@ TileLoop tiles_of(int64_t n) {
   TileLoop T;
   T.nb = n / FP4Q_BLOCK;
   T.tiles = (T.nb + kTileBlocks - 1) / kTileBlocks;
+  T.bpr = 0;
   T.negzero = -0.0f;
   return T;
 }
@@ -1550,6 +1623,58 @@ fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) 
   return launch_tail(tail_roundtrip_kernel<G, F, MX, XF>, s,
                      static_cast<const void*>(static_cast<const uint8_t*>(x) + nfull * es),
                      static_cast<void*>(static_cast<uint8_t*>(y) + nfull * es), (int)(n - nfull), -0.0f);
+}
+
+// Strided 2-D launches (rows x cols, cols a multiple of 256, row strides in elements).
+// The kernels are the contiguous ones; only the tensor maps and TileLoop.bpr differ.
+TileLoop tiles_2d(int64_t rows, int64_t cols) {
+  TileLoop T = tiles_of(rows * cols);
+  T.bpr = cols / FP4Q_BLOCK;
+  return T;
+}
+
+template <int G, int F, bool MX>
+fp4q_status launch_compress_2d(const void* x, int64_t rows, int64_t cols, int64_t ld, void* payload, cudaStream_t s) {
+  const TileLoop T = tiles_2d(rows, cols);
+  CUtensorMap xm;
+  if (!rows_map(&xm, x, rows, cols, ld, false)) return FP4Q_ERR_CUDA;
+  auto k = compress_kernel<G, F, MX, false>;
+  Launch L;
+  fp4q_status st = plan(k, kCompressWarps, WarpSmemLayout<kCompressWarps, kCompressStages, 4096>::kCtaBytes,
+                        T.tiles, L);
+  if (st != FP4Q_OK) return st;
+  return launch_pdl(k, L, kCompressWarps * 32, s, xm, payload_of(payload, rows * cols, G, MX), T);
+}
+
+template <int G, int F, int DT, int B, bool MX>
+fp4q_status launch_decompress_2d(const void* payload, int64_t rows, int64_t cols, void* dst, int64_t ld,
+                                 cudaStream_t s) {
+  const TileLoop T = tiles_2d(rows, cols);
+  CUtensorMap dm;
+  if (!rows_map(&dm, dst, rows, cols, ld, DT == FP4Q_F32)) return FP4Q_ERR_CUDA;
+  auto k = decompress_kernel<G, F, DT, B, MX>;
+  constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
+  Launch L;
+  fp4q_status st = plan(k, kDecompressWarps,
+                        WarpSmemLayout<kDecompressWarps, kDecompressStages, B ? TB : 0>::kCtaBytes, T.tiles, L,
+                        kDecompressGridCtas);
+  if (st != FP4Q_OK) return st;
+  return launch_pdl(k, L, kDecompressWarps * 32, s, dm,
+                    payload_of(const_cast<void*>(payload), rows * cols, G, MX), T);
+}
+
+template <int G, int F, bool MX>
+fp4q_status launch_roundtrip_2d(const void* x, int64_t rows, int64_t cols, int64_t ldx, void* y, int64_t ldy,
+                                cudaStream_t s) {
+  const TileLoop T = tiles_2d(rows, cols);
+  CUtensorMap xm, ym;
+  if (!rows_map(&xm, x, rows, cols, ldx, false) || !rows_map(&ym, y, rows, cols, ldy, false)) return FP4Q_ERR_CUDA;
+  auto k = roundtrip_kernel<G, F, MX, false>;
+  Launch L;
+  fp4q_status st = plan(k, kRoundtripWarps, WarpSmemLayout<kRoundtripWarps, kRoundtripStages, 4096>::kCtaBytes,
+                        T.tiles, L);
+  if (st != FP4Q_OK) return st;
+  return launch_pdl(k, L, kRoundtripWarps * 32, s, xm, ym, T);
 }
 
 template <int G, int R, bool MX>
@@ -1638,6 +1763,19 @@ fp4q_status roundtrip_entry(const void* x, int64_t n, void* y, const fp4q_params
   return F ? launch_roundtrip<32, 1, false, XF>(x, n, y, s) : launch_roundtrip<32, 0, false, XF>(x, n, y, s);
 }
 
+// A strided 2-D view: rows >= 1, cols a positive multiple of 256, rows * cols < 2^37,
+// cols <= ld < 2^37 with 16-byte aligned rows (ld * element size a multiple of 16).
+fp4q_status check_2d(int64_t rows, int64_t cols, int64_t ld, int esz) {
+  const int64_t lim = (int64_t)1 << 37;
+  if (rows < 1 || cols < FP4Q_BLOCK || cols % FP4Q_BLOCK != 0 || cols >= lim || rows >= lim / cols)
+    return FP4Q_ERR_SIZE;
+  if (ld < cols || ld >= lim) return FP4Q_ERR_PARAM;
+  if ((ld * esz) % 16 != 0) return FP4Q_ERR_ALIGN;
+  return FP4Q_OK;
+}
+// Bytes spanned by a strided view.
+size_t span_2d(int64_t rows, int64_t cols, int64_t ld, int esz) { return (size_t)((rows - 1) * ld + cols) * esz; }
+
 }  // namespace
 
 extern "C" {
@@ -1700,6 +1838,81 @@ fp4q_status fp4q_roundtrip(const void* x_bf16, int64_t n, void* y_bf16, const fp
 fp4q_status fp4q_roundtrip_f32(const void* x_f32, int64_t n, void* y_f32, const fp4q_params* params,
                                void* stream) {
   return roundtrip_entry<true>(x_f32, n, y_f32, params, stream);
+}
+
+fp4q_status fp4q_compress_2d(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld, void* payload,
+                             const fp4q_params* params, void* stream) {
+  int G, F;
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
+  if (st != FP4Q_OK) return st;
+  if (!x_bf16 || !payload) return FP4Q_ERR_NULL;
+  if ((st = check_2d(rows, cols, ld, 2)) != FP4Q_OK) return st;
+  if (!aligned16(x_bf16) || !aligned16(payload)) return FP4Q_ERR_ALIGN;
+  const int64_t n = rows * cols;
+  if (overlap(x_bf16, span_2d(rows, cols, ld, 2), payload, payload_bytes_of(n, G, MX))) return FP4Q_ERR_OVERLAP;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ld == cols) return fp4q_compress(x_bf16, n, payload, params, stream);
+  if (MX) return F ? launch_compress_2d<32, 1, true>(x_bf16, rows, cols, ld, payload, s)
+                   : launch_compress_2d<32, 0, true>(x_bf16, rows, cols, ld, payload, s);
+  if (G == 16) return F ? launch_compress_2d<16, 1, false>(x_bf16, rows, cols, ld, payload, s)
+                        : launch_compress_2d<16, 0, false>(x_bf16, rows, cols, ld, payload, s);
+  return F ? launch_compress_2d<32, 1, false>(x_bf16, rows, cols, ld, payload, s)
+           : launch_compress_2d<32, 0, false>(x_bf16, rows, cols, ld, payload, s);
+}
+
+fp4q_status fp4q_decompress_accumulate_2d(const void* payload, int64_t rows, int64_t cols, void* dst, int64_t ld,
+                                          fp4q_dtype dtype, int32_t beta, const fp4q_params* params,
+                                          void* stream) {
+  int G, F;
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
+  if (st != FP4Q_OK) return st;
+  if ((dtype != FP4Q_BF16 && dtype != FP4Q_F32) || (beta != 0 && beta != 1)) return FP4Q_ERR_PARAM;
+  if (!payload || !dst) return FP4Q_ERR_NULL;
+  const int esz = dtype == FP4Q_BF16 ? 2 : 4;
+  if ((st = check_2d(rows, cols, ld, esz)) != FP4Q_OK) return st;
+  if (!aligned16(payload) || !aligned16(dst)) return FP4Q_ERR_ALIGN;
+  const int64_t n = rows * cols;
+  if (overlap(payload, payload_bytes_of(n, G, MX), dst, span_2d(rows, cols, ld, esz))) return FP4Q_ERR_OVERLAP;
+  if (ld == cols) return fp4q_decompress_accumulate(payload, n, dst, dtype, beta, params, stream);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int key = F * 4 + (dtype == FP4Q_F32) * 2 + beta;
+#define FP4Q_D2(GG, MM)                                                                        \
+  switch (key) {                                                                               \
+    case 0: return launch_decompress_2d<GG, 0, FP4Q_BF16, 0, MM>(payload, rows, cols, dst, ld, s); \
+    case 1: return launch_decompress_2d<GG, 0, FP4Q_BF16, 1, MM>(payload, rows, cols, dst, ld, s); \
+    case 2: return launch_decompress_2d<GG, 0, FP4Q_F32, 0, MM>(payload, rows, cols, dst, ld, s);  \
+    case 3: return launch_decompress_2d<GG, 0, FP4Q_F32, 1, MM>(payload, rows, cols, dst, ld, s);  \
+    case 4: return launch_decompress_2d<GG, 1, FP4Q_BF16, 0, MM>(payload, rows, cols, dst, ld, s); \
+    case 5: return launch_decompress_2d<GG, 1, FP4Q_BF16, 1, MM>(payload, rows, cols, dst, ld, s); \
+    case 6: return launch_decompress_2d<GG, 1, FP4Q_F32, 0, MM>(payload, rows, cols, dst, ld, s);  \
+    default: return launch_decompress_2d<GG, 1, FP4Q_F32, 1, MM>(payload, rows, cols, dst, ld, s); \
+  }
+  if (MX) FP4Q_D2(32, true)
+  if (G == 16) FP4Q_D2(16, false)
+  FP4Q_D2(32, false)
+#undef FP4Q_D2
+}
+
+fp4q_status fp4q_roundtrip_2d(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, void* y_bf16,
+                              int64_t ldy, const fp4q_params* params, void* stream) {
+  int G, F;
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
+  if (st != FP4Q_OK) return st;
+  if (!x_bf16 || !y_bf16) return FP4Q_ERR_NULL;
+  if ((st = check_2d(rows, cols, ldx, 2)) != FP4Q_OK || (st = check_2d(rows, cols, ldy, 2)) != FP4Q_OK) return st;
+  if (!aligned16(x_bf16) || !aligned16(y_bf16)) return FP4Q_ERR_ALIGN;
+  if (overlap(x_bf16, span_2d(rows, cols, ldx, 2), y_bf16, span_2d(rows, cols, ldy, 2))) return FP4Q_ERR_OVERLAP;
+  if (ldx == cols && ldy == cols) return fp4q_roundtrip(x_bf16, rows * cols, y_bf16, params, stream);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (MX) return F ? launch_roundtrip_2d<32, 1, true>(x_bf16, rows, cols, ldx, y_bf16, ldy, s)
+                   : launch_roundtrip_2d<32, 0, true>(x_bf16, rows, cols, ldx, y_bf16, ldy, s);
+  if (G == 16) return F ? launch_roundtrip_2d<16, 1, false>(x_bf16, rows, cols, ldx, y_bf16, ldy, s)
+                        : launch_roundtrip_2d<16, 0, false>(x_bf16, rows, cols, ldx, y_bf16, ldy, s);
+  return F ? launch_roundtrip_2d<32, 1, false>(x_bf16, rows, cols, ldx, y_bf16, ldy, s)
+           : launch_roundtrip_2d<32, 0, false>(x_bf16, rows, cols, ldx, y_bf16, ldy, s);
 }
 
 fp4q_status fp4q_reduce_requantize(const void* const* payloads, int32_t R, int64_t n, void* out_payload,

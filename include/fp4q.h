@@ -173,6 +173,22 @@ fp4q_status fp4q_roundtrip(const void* x_bf16, int64_t n, void* y_bf16,
 fp4q_status fp4q_roundtrip_f32(const void* x_f32, int64_t n, void* y_f32,
                                const fp4q_params* params, void* stream);
 
+/* Strided 2-D variants (general shapes): a row-major [rows, cols] view with a row stride of
+ * ld elements (ld >= cols, ld * element size a multiple of 16 bytes, cols a multiple of
+ * 256, rows * cols < 2^37). The payload is that of the dense row-major [rows, cols] tensor
+ * (n = rows * cols) and is interchangeable with the 1-D entry points'; only the data
+ * tensors are strided. Each block is one TMA box of a 3-D map {line, line in row, row}.
+ * Errors as for the 1-D calls; a bad shape gives FP4Q_ERR_SIZE, ld < cols FP4Q_ERR_PARAM,
+ * a misaligned row stride FP4Q_ERR_ALIGN. ld == cols runs the 1-D call. */
+fp4q_status fp4q_compress_2d(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
+                             void* payload, const fp4q_params* params, void* stream);
+fp4q_status fp4q_decompress_accumulate_2d(const void* payload, int64_t rows, int64_t cols,
+                                          void* dst, int64_t ld, fp4q_dtype dtype, int32_t beta,
+                                          const fp4q_params* params, void* stream);
+fp4q_status fp4q_roundtrip_2d(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx,
+                              void* y_bf16, int64_t ldy, const fp4q_params* params,
+                              void* stream);
+
 /* Emulated R-way reduce: payloads is a HOST array of R device pointers, each a payload of
  * n elements made with the same params; out_payload (device) receives the requantized sum
  * (Reduce step above). This is the fused decompress-sum-requantize step of a

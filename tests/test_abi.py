@@ -170,3 +170,21 @@ def test_f32_entry_points_argument_errors(L):
     # overlaps (it would not for a BF16 input of the same n)
     assert L.fp4q_compress_f32(A, 4096, A + 2 * 4096 + 16, pp, None) == _lib.ERR_OVERLAP
     assert L.fp4q_roundtrip_f32(A, 4096, A + 4 * 4096 - 16, pp, None) == _lib.ERR_OVERLAP
+
+
+def test_2d_entry_points_argument_errors(L):
+    pp = ctypes.byref(P)
+    c2, d2, r2 = L.fp4q_compress_2d, L.fp4q_decompress_accumulate_2d, L.fp4q_roundtrip_2d
+    assert c2(None, 4, 512, 1024, B, pp, None) == _lib.ERR_NULL
+    for rows, cols in [(0, 512), (4, 0), (4, 300), (4, 100), (1 << 30, 1 << 10)]:
+        assert c2(A, rows, cols, 4096, B, pp, None) == _lib.ERR_SIZE, (rows, cols)
+    assert c2(A, 4, 512, 256, B, pp, None) == _lib.ERR_PARAM          # ld < cols
+    assert c2(A, 4, 512, 1 << 40, B, pp, None) == _lib.ERR_PARAM
+    assert c2(A, 4, 512, 516, B, pp, None) == _lib.ERR_ALIGN          # 1032-byte rows
+    assert c2(A, 4, 512, 520, B + 8, pp, None) == _lib.ERR_ALIGN
+    # the view spans (rows - 1) * ld + cols elements: a payload inside the last row overlaps
+    assert c2(A, 4, 512, 1024, A + 2 * (3 * 1024 + 128), pp, None) == _lib.ERR_OVERLAP
+    assert d2(A, 4, 512, B, 514, _lib.F32, 1, pp, None) == _lib.ERR_ALIGN   # 2056-byte f32 rows
+    assert d2(A, 4, 512, B, 1024, 7, 1, pp, None) == _lib.ERR_PARAM
+    assert r2(A, 4, 512, 1024, B, 256, pp, None) == _lib.ERR_PARAM
+    assert r2(A, 4, 512, 1024, A + 1024, 1024, pp, None) == _lib.ERR_OVERLAP
