@@ -6,7 +6,8 @@
 Each kernel is timed alone with CUDA events on the launching stream, after an L2 flush
 (a write of a buffer larger than L2 followed by a read of another one), and reported as
 algorithmic GB/s (the bytes the kernel must move, G = 16; the *_mx kernels use the E8M0
-variant, group 32; compress_f32 / roundtrip_f32 take FP32 input) and as a fraction of the measured
+variant, group 32; compress_f32 / roundtrip_f32 take FP32 input; compress_2d reads a strided
+[n/4096, 4096] view of an [n/4096, 8192] matrix) and as a fraction of the measured
 HBM copy bandwidth in MEASURED_PEAKS.json when that file is present. Inputs are N(0,1)
 bfloat16 tensors made on the device (timing only; parity is the tests' business).
 """
@@ -39,6 +40,7 @@ ALG_BYTES = {
     "reduce_mx_r4": 5 * PAYLOAD_MX,
     "compress_f32": 4 + PAYLOAD,
     "roundtrip_f32": 8.0,
+    "compress_2d": 2 + PAYLOAD,
 }
 
 
@@ -91,6 +93,10 @@ def main():
         f32 = any(k in ("compress_f32", "roundtrip_f32") for k in args.kernels)
         xf = x.float() if f32 else None
         yf = torch.empty_like(xf) if f32 else None
+        # rows of 4096 elements every 8192: the left half of a twice wider matrix
+        wide = torch.empty(n // 4096, 8192, dtype=torch.bfloat16, device=dev) if "compress_2d" in args.kernels else None
+        if wide is not None:
+            wide[:, :4096] = x.view(-1, 4096)
         pm = [fq.compress(x * (r + 1), scales="e8m0") for r in range(4)] if mx else None
         outm = torch.empty_like(pm[0]) if mx else None
         fns = {
@@ -109,13 +115,14 @@ def main():
             "reduce_mx_r4": lambda: fq.reduce_requantize(pm[:4], n, out=outm, scales="e8m0"),
             "compress_f32": lambda: fq.compress(xf, payload=ps[0]),
             "roundtrip_f32": lambda: fq.roundtrip(xf, y=yf),
+            "compress_2d": lambda: fq.compress(wide[:, :4096], payload=ps[0]),
         }
         for k in args.kernels:
             t = timed(fns[k])
             gbs = ALG_BYTES[k] * n / t / 1e9
             print(json.dumps({"n": n, "kernel": k, "us": round(t * 1e6, 2), "alg_gbs": round(gbs, 1),
                               "frac_of_peak": None if not peak else round(gbs / peak, 4)}), flush=True)
-        del x, ps, d16, d32, y, out, pm, outm, xf, yf
+        del x, ps, d16, d32, y, out, pm, outm, xf, yf, wide
 
 
 if __name__ == "__main__":
