@@ -53,7 +53,7 @@ constexpr int kCompressWarps = 4, kCompressStages = 1, kCompressCtas = 4;
 constexpr int kRoundtripWarps = 4, kRoundtripStages = 1, kRoundtripCtas = 4;
 constexpr int kDecompressWarps = 4, kDecompressStages = 1, kDecompressCtas = 4;
 constexpr int kDecompressGridCtas = 4;     // resident CTAs per SM the grid is sized for
-constexpr int kReduceWarps = 4, kReduceCtas = 4;
+constexpr int kReduceWarps = 4;
 constexpr float kZeroLimit = 2688.0f * 0x1p-100f;   // all-zero block guard on A_b
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -1152,14 +1152,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 template <int R>
 struct ReduceCfg {
-  static constexpr int kStagesR = R <= 4 ? 3 : 2;
+  static constexpr int kStagesR = R <= 4 ? 2 : 1;
+  static constexpr int kMinCtas = 4;                                 // launch bound: CTAs per SM
   static constexpr int kStageBytes = R * kRankStageBytes;
   static constexpr int kRegion = kStagesR * kStageBytes + 128;       // + barriers
   static constexpr int kCtaBytes = kReduceWarps * kRegion + 128;
 };
 
 template <int G, int R, bool MX>
-__global__ void __launch_bounds__(kReduceWarps * 32, kReduceCtas)
+__global__ void __launch_bounds__(kReduceWarps * 32, ReduceCfg<R>::kMinCtas)
 reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
   typedef ReduceCfg<R> C;
   extern __shared__ uint8_t smem_raw[];
