@@ -891,14 +891,16 @@ struct TileLoop {
   int64_t tiles;     // number of 8-block tiles
   int64_t nb;        // number of 256-element blocks
   int64_t bpr;       // 0: the data tensor is contiguous; else blocks per row of a strided 2-D tensor
+  int64_t tpr;       // strided rows holding whole tiles (bpr % 8 == 0): tiles per row, else 0
   float negzero;     // -0.0f, set by the host so the compiler cannot see its value
 };
 
 // TMA traffic of one tile of a data tensor (x, y or dst) with LPB 128-byte lines per block
 // (4 for BF16, 8 for FP32). Contiguous data is a 2-D map of lines and a tile is one box;
-// a strided 2-D tensor is a 3-D map {line, line in row, row} and a tile is one box per
-// existing block (blocks never straddle rows: cols is a multiple of 256). Each block lands
-// at the same shared-memory offset either way, so the swizzled tile layout is unchanged.
+// a strided 2-D tensor is a 3-D map {line, line in row, row} and a tile is one box when rows
+// hold whole tiles (tpr), else one box per existing block (blocks never straddle rows: cols
+// is a multiple of 256). Each block lands at the same shared-memory offset either way, so
+// the swizzled tile layout is unchanged.
 template <int LPB>
 __device__ __forceinline__ void tile_load(const CUtensorMap* map, const TileLoop& T, int64_t t, uint32_t buf,
                                           uint32_t bar) {
@@ -906,6 +908,12 @@ __device__ __forceinline__ void tile_load(const CUtensorMap* map, const TileLoop
   if (T.bpr == 0) {
     mbar_expect_tx(bar, kTileBlocks * BPB);
     tma_load_2d(buf, map, 0, (int32_t)(t * kTileBlocks * LPB), bar);
+    return;
+  }
+  if (T.tpr) {
+    const int64_t row = t / T.tpr;
+    mbar_expect_tx(bar, kTileBlocks * BPB);
+    tma_load_3d(buf, map, 0, (int32_t)((t - row * T.tpr) * kTileBlocks * LPB), (int32_t)row, bar);
     return;
   }
   const int64_t gb0 = t * kTileBlocks;
@@ -928,6 +936,11 @@ __device__ __forceinline__ void tile_store(const CUtensorMap* map, const TileLoo
   constexpr uint32_t BPB = 128u * LPB;
   if (T.bpr == 0) {
     tma_store_2d(map, 0, (int32_t)(t * kTileBlocks * LPB), src);
+    return;
+  }
+  if (T.tpr) {
+    const int64_t row = t / T.tpr;
+    tma_store_3d(map, 0, (int32_t)((t - row * T.tpr) * kTileBlocks * LPB), (int32_t)row, src);
     return;
   }
   const int64_t gb0 = t * kTileBlocks;
@@ -1544,12 +1557,14 @@ bool line_map(CUtensorMap* m, const void* ptr, int64_t n, bool f32) {
 // Strided 2-D tensor [rows, cols] with row stride ld elements, as a 3-D map of 128-byte
 // lines {line, line in row, row}; one box is one 256-element block.
 bool rows_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool f32) {
+  // one box per tile when whole tiles fit in a row (cols a multiple of 2048), else per block
+  const bool tiles = cols % (kTileBlocks * FP4Q_BLOCK) == 0;
   EncodeTiled enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t per_line = f32 ? 32 : 64, esz = f32 ? 4 : 2;
   const cuuint64_t dims[3] = {per_line, (cuuint64_t)cols / per_line, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {128, (cuuint64_t)ld * esz};
-  const cuuint32_t box[3] = {(cuuint32_t)per_line, f32 ? 8u : 4u, 1u};
+  const cuuint32_t box[3] = {(cuuint32_t)per_line, (f32 ? 8u : 4u) * (tiles ? (cuuint32_t)kTileBlocks : 1u), 1u};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1586,6 +1601,7 @@ TileLoop tiles_of(int64_t n) {
   T.nb = n / FP4Q_BLOCK;
   T.tiles = (T.nb + kTileBlocks - 1) / kTileBlocks;
   T.bpr = 0;
+  T.tpr = 0;
   T.negzero = -0.0f;
   return T;
 }
@@ -1670,6 +1686,7 @@ fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) 
 TileLoop tiles_2d(int64_t rows, int64_t cols) {
   TileLoop T = tiles_of(rows * cols);
   T.bpr = cols / FP4Q_BLOCK;
+  T.tpr = T.bpr % kTileBlocks == 0 ? T.bpr / kTileBlocks : 0;
   return T;
 }
 
