@@ -19,7 +19,7 @@ _SRC = os.path.join(_PKG, "csrc", "fp4q.cu")
 _HDR = os.path.join(_ROOT, "include", "fp4q.h")
 LIB_PATH = os.path.join(_PKG, f"libfp4q_{platform.machine()}.so")
 
-NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-fmad=false",
+NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-fmad=false", "-split-compile=0",
               "-std=c++17", "-Xcompiler", "-fPIC", "-shared"]
 
 # status codes (fp4q_status)
