@@ -54,6 +54,11 @@ constexpr int kRoundtripWarps = 4, kRoundtripStages = 1, kRoundtripCtas = 4;
 constexpr int kDecompressWarps = 4, kDecompressStages = 1, kDecompressCtas = 4;
 constexpr int kDecompressGridCtas = 4;     // resident CTAs per SM the grid is sized for
 constexpr int kReduceWarps = 4;
+// Large reduces (at least kReduceDynTilesPerSm tiles per SM) run one CTA of
+// kReduceDynWarps warps per SM with dynamic tile claims (InPipe DYN): warps of one SM were
+// measured finishing up to 9 us apart under the round-robin assignment.
+constexpr int kReduceDynWarps = 16;
+constexpr int64_t kReduceDynTilesPerSm = 384;
 constexpr float kZeroLimit = 2688.0f * 0x1p-100f;   // all-zero block guard on A_b
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -717,13 +722,26 @@ __device__ __forceinline__ WarpSmem warp_smem(uint8_t* raw, int warp) {
 // Per-warp input pipeline over STAGES stage buffers of BYTES bytes: STAGES tiles stay in
 // flight (issue(buf, bar, t) arms the barrier and starts the copies of tile t; lane 0 calls
 // it, or every lane when ALL_LANES, for copies spread over lanes); every lane waits on the
-// tile's barrier, reads the stage, and the stage is refilled with the tile STAGES
-// iterations ahead.
-template <int STAGES, int BYTES, bool ALL_LANES = false>
+// tile's barrier, reads the stage, and the stage is refilled with the warp's next tile.
+// Tiles come round robin (warp w of W takes w, w + W, ...), or with DYN from the CTA's
+// claim counter in shared memory: CTA c's tiles are c, c + G, c + 2G, ... (G = gridDim.x)
+// and its warps take them in the order they ask, so warps that run ahead do more tiles.
+template <int STAGES, int BYTES, bool ALL_LANES = false, bool DYN = false>
 struct InPipe {
   uint32_t stage0, bar0;
   int64_t t0, W, tiles;
   int i, issued;
+  uint32_t ctr, asked;          // DYN: the CTA's counter (shared address), lane 0's claim
+  int64_t tid[DYN ? STAGES : 1];  // DYN: the tile each stage holds
+
+  __device__ __forceinline__ int64_t claim_tile(uint32_t claim) const {
+    return (int64_t)blockIdx.x + (int64_t)__shfl_sync(kFull, claim, 0) * gridDim.x;
+  }
+  __device__ __forceinline__ uint32_t claim_ask(int lane) const {
+    uint32_t c = 0;
+    if (lane == 0) asm volatile("atom.shared.add.u32 %0, [%1], 1;" : "=r"(c) : "r"(ctr) : "memory");
+    return c;
+  }
 
   __device__ __forceinline__ uint32_t buf(int s) const { return stage0 + (uint32_t)(s * BYTES); }
   __device__ __forceinline__ uint32_t bar(int s) const { return bar0 + 8u * (uint32_t)s; }
@@ -751,6 +769,42 @@ struct InPipe {
     }
     i = 0;
   }
+  // DYN start: the CTA's counter at shared address ctr_ (zeroed, with a CTA barrier, by
+  // dyn_counter_init before any warp gets here).
+  template <class Issue>
+  __device__ __forceinline__ void start_dyn(uint32_t stage0_, uint32_t bar0_, uint32_t ctr_, int64_t tiles_, int lane,
+                                            Issue&& issue) {
+    static_assert(DYN, "start_dyn needs DYN");
+    stage0 = stage0_;
+    bar0 = bar0_;
+    ctr = ctr_;
+    tiles = tiles_;
+    if (lane == 0) {
+      for (int s = 0; s < STAGES; ++s) mbar_init(bar(s), 1);
+      fence_barrier_init();
+    }
+    __syncwarp();
+    issued = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      tid[s] = claim_tile(claim_ask(lane));
+      if (tid[s] < tiles) {
+        if (ALL_LANES || lane == 0) issue(buf(s), bar(s), tid[s]);
+        ++issued;
+      }
+    }
+    i = 0;
+  }
+  // The current tile and the one after it.
+  __device__ __forceinline__ int64_t tile() const { return DYN ? tid[i % STAGES] : t0 + (int64_t)i * W; }
+  __device__ __forceinline__ int64_t next_tile() const {
+    static_assert(!DYN || STAGES > 1, "with one stage the next tile is claimed at the refill");
+    return DYN ? tid[(i + 1) % STAGES] : t0 + (int64_t)(i + 1) * W;
+  }
+  // DYN: claim the tile the next refill loads, at the top of an iteration, so the counter's
+  // latency hides behind the wait and the reading of the stage.
+  __device__ __forceinline__ void ask(int lane) {
+    if (DYN) asked = claim_ask(lane);
+  }
   __device__ __forceinline__ uint32_t cur() const { return buf(i % STAGES); }
   // Wait for the current tile. On failure record the fault, wait (bounded) for every copy
   // still in flight into this warp's stages, and return false: the caller must stop.
@@ -773,7 +827,8 @@ struct InPipe {
   __device__ __forceinline__ void refill(int lane, Issue&& issue) {
     fence_proxy_async();
     __syncwarp();
-    const int64_t tn = t0 + (int64_t)(i + STAGES) * W;
+    const int64_t tn = DYN ? claim_tile(asked) : t0 + (int64_t)(i + STAGES) * W;
+    if (DYN) tid[i % STAGES] = tn;
     if (tn < tiles) {
       if (ALL_LANES || lane == 0) issue(buf(i % STAGES), bar(i % STAGES), tn);
       ++issued;
@@ -956,6 +1011,12 @@ __device__ __forceinline__ void tile_store(const CUtensorMap* map, const TileLoo
       ++row;
     }
   }
+}
+
+// Zero a CTA's tile counter before any warp claims from it.
+__device__ __forceinline__ void dyn_counter_init(uint32_t ctr) {
+  if (threadIdx.x == 0) asm volatile("st.shared.u32 [%0], 0;" ::"r"(ctr) : "memory");
+  __syncthreads();
 }
 
 template <int WARPS>
@@ -1175,13 +1236,14 @@ struct ReduceCfg {
   static constexpr bool kDirectScales = kReduceDirectScales && R >= 3 && R <= 4;
   static constexpr int kStagesR = R <= 4 ? 2 : 1;
   static constexpr int kMinCtas = 4;                                 // launch bound: CTAs per SM
+  static constexpr int cta_bytes(int warps) { return warps * kRegion + 128 + 16; }   // + DYN counter
   static constexpr int kStageBytes = R * kRankStageBytes;
   static constexpr int kRegion = kStagesR * kStageBytes + 128;       // + barriers
-  static constexpr int kCtaBytes = kReduceWarps * kRegion + 128;
+
 };
 
-template <int G, int R, bool MX>
-__global__ void __launch_bounds__(kReduceWarps * 32, ReduceCfg<R>::kMinCtas)
+template <int G, int R, bool MX, bool DYN>
+__global__ void __launch_bounds__(DYN ? kReduceDynWarps * 32 : kReduceWarps * 32, DYN ? 1 : ReduceCfg<R>::kMinCtas)
 reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
   typedef ReduceCfg<R> C;
   constexpr bool DS = C::kDirectScales && !MX;
@@ -1233,12 +1295,19 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
       sb[r] = (!ok || MX) ? 0.0f : __ldg(in.bsc[r] + b);
     }
   };
-  InPipe<C::kStagesR, C::kStageBytes, true> pipe{};
-  pipe.start(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), warp_global<kReduceWarps>(),
-             warp_count<kReduceWarps>(), T.tiles, lane, issue);
-  if (DS) load_scales(pipe.t0, cg, cs);
-  for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
-    if (DS) load_scales(t + pipe.W, ng, ns);
+  InPipe<C::kStagesR, C::kStageBytes, true, DYN> pipe{};
+  if constexpr (DYN) {
+    const uint32_t ctr = ((smem_addr(smem_raw) + 127u) & ~127u) + (uint32_t)(kReduceDynWarps * C::kRegion);
+    dyn_counter_init(ctr);
+    pipe.start_dyn(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), ctr, T.tiles, lane, issue);
+  } else {
+    pipe.start(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), warp_global<kReduceWarps>(),
+               warp_count<kReduceWarps>(), T.tiles, lane, issue);
+  }
+  if (DS) load_scales(DYN ? pipe.tile() : pipe.t0, cg, cs);
+  for (int64_t t = DYN ? pipe.tile() : pipe.t0; t < T.tiles; t = DYN ? pipe.tile() : t + pipe.W) {
+    pipe.ask(lane);
+    if constexpr (DS) load_scales(DYN ? pipe.next_tile() : t + pipe.W, ng, ns);
     const int64_t gb = t * kTileBlocks + blk;
     const bool valid = gb < T.nb;
     // a block scale outside the bulk-copied whole 16-byte units of the last tile
@@ -1738,11 +1807,15 @@ template <int G, int R, bool MX>
 fp4q_status launch_reduce_r(const RankPtrs& in, int64_t n, void* out, cudaStream_t s) {
   n = padded_n(n);   // the reduce works on whole (zero-padded) blocks of the payloads
   TileLoop T = tiles_of(n);
-  auto k = reduce_kernel<G, R, MX>;
+  const Payload P = payload_of(out, n, G, MX);
+  const int sms = num_sms();
+  const bool dyn = sms > 0 && T.tiles >= kReduceDynTilesPerSm * sms;
+  auto k = dyn ? reduce_kernel<G, R, MX, true> : reduce_kernel<G, R, MX, false>;
+  const int warps = dyn ? kReduceDynWarps : kReduceWarps;
   Launch L;
-  fp4q_status st = plan(k, kReduceWarps, ReduceCfg<R>::kCtaBytes, T.tiles, L);
+  fp4q_status st = plan(k, warps, ReduceCfg<R>::cta_bytes(warps), T.tiles, L);
   if (st != FP4Q_OK) return st;
-  return launch_pdl(k, L, kReduceWarps * 32, s, in, payload_of(out, n, G, MX), T);
+  return launch_pdl(k, L, warps * 32, s, in, P, T);
 }
 
 template <int G, bool MX>
