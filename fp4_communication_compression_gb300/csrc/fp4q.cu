@@ -15,9 +15,19 @@
 //   layout B: lane (L & 3) = b holds rows b, b+4, b+8, b+12 (all p, g bits 2-3 in registers)
 // Values are kept as float2 pairs (p even, p odd) so that the butterflies run on the
 // packed FP32x2 pipe (add/sub/mul.rn.f32x2). FWHT strides 1..32 act on layout A, strides
-// 64 and 128 on layout B; one transpose through a padded, bank-conflict-free shared buffer
-// (73 16-byte units per block) moves between them. Group and block maxima reduce over the
-// 4 lanes of a block with two xor-shuffles.
+// 64 and 128 on layout B; one transpose through an unpadded, XOR-swizzled, bank-conflict-
+// free shared buffer (1 KiB per block) moves between them. Group and block maxima reduce
+// over the 4 lanes of a block with two xor-shuffles.
+//
+// Data movement and scheduling. Each warp streams its tiles through its own TMA pipeline
+// (InPipe: mbarrier-tracked cp.async.bulk.tensor loads with bounded waits), and BF16 / FP32
+// outputs leave by TMA stores from a swizzled staging buffer. Tiles are assigned round robin
+// to the warps of the grid; large reduces instead run one CTA per SM whose warps claim tiles
+// from a shared-memory counter. Every kernel starts with griddepcontrol.wait and is launched
+// with programmatic stream serialisation, so back-to-back codec kernels overlap launch and
+// drain. The same kernels serve the E8M0 (microscaled) scales, FP32 input, strided 2-D
+// views (3-D tensor maps) and, through one-warp tail kernels, lengths that are not a
+// multiple of 256.
 //
 // Exactness. Every floating-point step is a separately rounded FP32 operation: the file is
 // built with -fmad=false, packed ops carry .rn, no operation is reassociated, and the scale
@@ -25,7 +35,8 @@
 // fp4q_math.cuh (checked exhaustively against CUDA's IEEE __fdiv_rn / __frcp_rn over the
 // operand ranges used here). Two rewrites are bit-identical to the contract's literal order
 // and are used to save work:
-//   * compress never multiplies y by 1/16: max|y| = fl(max|z| / 16) because rounding is
+//   * with dual scales compress never multiplies y by 1/16 (the E8M0 path does, since its
+//     power-of-two scale would expose the difference): max|y| = fl(max|z| / 16) because rounding is
 //     monotone, and q = y * inv = z * (inv / 16) exactly whenever a code can depend on it
 //     (inv / 16 is exact for |x| < 2^120; a y that underflows gives |q| < 2^-17, code +-0
 //     with the sign of z either way);
