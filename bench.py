@@ -78,12 +78,17 @@ def measured_peak():
 
 
 def kernel_source_sha() -> str:
-    """Hash of everything the kernels are built from (csrc/*.cu, csrc/*.cuh, include/fp4q.h)."""
+    """Hash of the code the kernels are built from (csrc/*.cu, csrc/*.cuh, include/fp4q.h),
+    with comments and blank lines removed, so that editing a comment does not orphan the
+    ncu summaries taken on the same code."""
     csrc = os.path.join(ROOT, "fp4_communication_compression_gb300", "csrc")
     files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
     h = hashlib.sha256()
     for f in files + [os.path.join(ROOT, "include", "fp4q.h")]:
-        h.update(open(f, "rb").read())
+        text = open(f).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
     return h.hexdigest()[:16]
 
 
