@@ -15,9 +15,12 @@
 //   layout B: lane (L & 3) = b holds rows b, b+4, b+8, b+12 (all p, g bits 2-3 in registers)
 // Values are kept as float2 pairs (p even, p odd) so that the butterflies run on the
 // packed FP32x2 pipe (add/sub/mul.rn.f32x2). FWHT strides 1..32 act on layout A, strides
-// 64 and 128 on layout B; one transpose through an unpadded, XOR-swizzled, bank-conflict-
-// free shared buffer (1 KiB per block) moves between them. Group and block maxima reduce
-// over the 4 lanes of a block with two xor-shuffles.
+// 64 and 128 on layout B; one transpose through a bank-conflict-free shared buffer moves
+// between them. Compress and roundtrip move the two 8-column halves of a block one after
+// the other through a padded 640-byte buffer (each lane addresses it as one base plus
+// immediates, and the smaller buffer lets 5 CTAs share an SM); decompress and the tail
+// kernels use a 1 KiB-per-block XOR-swizzled buffer (reduce has no transform). Group and block maxima reduce over
+// the 4 lanes of a block with two xor-shuffles.
 //
 // Data movement and scheduling. Each warp streams its tiles through its own TMA pipeline
 // (InPipe: mbarrier-tracked cp.async.bulk.tensor loads with bounded waits), and BF16 / FP32
@@ -60,8 +63,11 @@ constexpr int kTileBlocks = 8;                  // 256-element blocks per warp t
 // Warps per CTA and input stages per warp, per kernel (shared memory per warp decides how
 // many warps fit on an SM: compress and roundtrip are issue/latency bound and want the
 // most resident warps; one stage is enough because a tile's compute outlasts its load).
-constexpr int kCompressWarps = 4, kCompressStages = 1, kCompressCtas = 4;
-constexpr int kRoundtripWarps = 4, kRoundtripStages = 1, kRoundtripCtas = 4;
+constexpr int kCompressWarps = 4, kCompressStages = 1, kCompressCtas = 5, kCompressCtasF32 = 4;
+// Compress and roundtrip grids that would give a warp fewer than kSmallGridTiles tiles at
+// their full CTAs per SM run kSmallGridCtas per SM instead (measured faster at 2^24 elements).
+constexpr int kSmallGridTiles = 3, kSmallGridCtas = 4;
+constexpr int kRoundtripWarps = 4, kRoundtripStages = 1, kRoundtripCtas = 5, kRoundtripCtasF32 = 4;
 constexpr int kDecompressWarps = 4, kDecompressStages = 1, kDecompressCtas = 4;
 constexpr int kDecompressGridCtas = 4;     // resident CTAs per SM the grid is sized for
 constexpr int kReduceWarps = 4;
@@ -284,6 +290,51 @@ __device__ __forceinline__ void transpose(Rows v, const XposeAddr& x) {
       v[k][2 * c + 1] = make_float2(__uint_as_float(t.z), __uint_as_float(t.w));
     }
   __syncwarp();
+}
+
+// Half-width transpose buffer: the two 8-column halves of every block go through it one
+// after the other, 640 bytes per block. Unit (row r = 4a + j, chunk cc of the half) is
+// stored at 10 a + 2 j + beta + cc (beta = block parity). The 8 lanes of an access phase
+// (two blocks, four lanes each) then hit 8 distinct 16-byte bank groups in layout A (lane a
+// writes its row j at 2a + beta + const mod 8) and in layout B (lane b reads its row k at
+// 2b + beta + const mod 8), and every unit is one per-lane base plus an immediate.
+constexpr int kXHalfBlockBytes = 640;
+
+struct XposeHalf {
+  uint32_t a, b;   // layout A base (unit 10 l4 + beta), layout B base (unit 2 l4 + beta)
+};
+
+__device__ __forceinline__ XposeHalf xpose_half_addr(uint32_t xbuf, int blk, int l4) {
+  const uint32_t blkb = xbuf + (uint32_t)blk * kXHalfBlockBytes, beta = (uint32_t)(blk & 1);
+  return {blkb + 16u * (10u * (uint32_t)l4 + beta), blkb + 16u * (2u * (uint32_t)l4 + beta)};
+}
+
+// transpose<toB> through the half-width buffer, one half of the columns at a time.
+template <bool toB>
+__device__ __forceinline__ void transpose_half(Rows v, const XposeHalf& x) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * h + cc;
+        sts128(toB ? x.a + 16u * (2 * k + cc) : x.b + 16u * (10 * k + cc),
+               make_uint4(__float_as_uint(v[k][2 * c].x), __float_as_uint(v[k][2 * c].y),
+                          __float_as_uint(v[k][2 * c + 1].x), __float_as_uint(v[k][2 * c + 1].y)));
+      }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * h + cc;
+        const uint4 t = lds128(toB ? x.b + 16u * (10 * k + cc) : x.a + 16u * (2 * k + cc));
+        v[k][2 * c] = make_float2(__uint_as_float(t.x), __uint_as_float(t.y));
+        v[k][2 * c + 1] = make_float2(__uint_as_float(t.z), __uint_as_float(t.w));
+      }
+    __syncwarp();
+  }
 }
 
 // ------------------------------------------------------------------ quantisation
@@ -704,14 +755,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 constexpr int kTileLinesBF16 = 32;         // 128-byte lines per 8-block bf16 tile (4 KiB)
 constexpr int kTileLinesF32 = 64;          // 128-byte lines per 8-block f32 tile (8 KiB)
 constexpr int kXBufBytes = 8192;           // transpose buffer / output staging per warp
+constexpr int kCompressXBytes = kTileBlocks * kXHalfBlockBytes;   // compress: half-width transpose
+// roundtrip: half-width transpose; the buffer also stages the output tile (8 KiB for FP32)
+template <bool XF>
+struct RoundtripXBytes {
+  static constexpr int value = XF ? kXBufBytes : kCompressXBytes;
+};
 constexpr int kHeaderBytes = 1024;         // per-CTA header: every warp's stage barriers
 
 // CTA shared memory: [alignment slack][header: 64 bytes of barriers per warp][warp regions],
-// each warp region = [input stages][xbuf], 1024-byte aligned (the 128-byte TMA swizzle
-// repeats every 1024 bytes).
-template <int WARPS, int STAGES, int IN_BYTES>
+// each warp region = [input stages][xbuf of XB bytes], 1024-byte aligned (the 128-byte TMA
+// swizzle repeats every 1024 bytes).
+template <int WARPS, int STAGES, int IN_BYTES, int XB = kXBufBytes>
 struct WarpSmemLayout {
-  static constexpr int kRegion = STAGES * IN_BYTES + kXBufBytes;
+  static constexpr int kRegion = STAGES * IN_BYTES + XB;
+  static_assert(kRegion % 1024 == 0, "warp regions must stay 1024-byte aligned");
   static constexpr int kCtaBytes = 1024 + kHeaderBytes + WARPS * kRegion;
 };
 
@@ -719,9 +777,9 @@ struct WarpSmem {
   uint32_t stage0, xbuf, bar0;
 };
 
-template <int STAGES, int IN_BYTES>
+template <int STAGES, int IN_BYTES, int XB = kXBufBytes>
 __device__ __forceinline__ WarpSmem warp_smem(uint8_t* raw, int warp) {
-  constexpr int region = STAGES * IN_BYTES + kXBufBytes;
+  constexpr int region = STAGES * IN_BYTES + XB;
   const uint32_t base = (smem_addr(raw) + 1023u) & ~1023u;
   WarpSmem w;
   w.stage0 = base + kHeaderBytes + (uint32_t)(warp * region);
@@ -1057,15 +1115,15 @@ __device__ __forceinline__ void staging_store(const CUtensorMap* map, const Tile
 // K1: compress. x (bfloat16, n) -> payload. Input tiles arrive by TMA.
 // XF: FP32 input (8 KiB tiles of 64 lines) instead of BF16 (4 KiB, 32 lines).
 template <int G, int FWHT, bool MX, bool XF>
-__global__ void __launch_bounds__(kCompressWarps * 32, kCompressCtas)
+__global__ void __launch_bounds__(kCompressWarps * 32, XF ? kCompressCtasF32 : kCompressCtas)
 compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T) {
   constexpr int IN = XF ? 8192 : 4096;
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  const WarpSmem ws = warp_smem<kCompressStages, IN>(smem_raw, warp);
-  const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
+  const WarpSmem ws = warp_smem<kCompressStages, IN, kCompressXBytes>(smem_raw, warp);
+  const XposeHalf xa = xpose_half_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<XF ? 8 : 4>(&xmap, T, t, buf, bar); };
   InPipe<kCompressStages, IN> pipe{};
   pipe.start(ws.stage0, ws.bar0, warp_global<kCompressWarps>(), warp_count<kCompressWarps>(), T.tiles, lane, issue);
@@ -1081,7 +1139,7 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
       level1_fwd_from2(v);
       rows_bfly(v, 1);             // h = 16
       rows_bfly(v, 2);             // h = 32
-      transpose<true>(v, xa);
+      transpose_half<true>(v, xa);
       rows_bfly(v, 1);             // h = 64
       rows_bfly(v, 2);             // h = 128
       if (MX) {
@@ -1163,15 +1221,15 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
 // K3: fused roundtrip. x (bfloat16) -> y = bf16(decode(compress(x))), no payload.
 // XF: FP32 input and output instead of BF16.
 template <int G, int FWHT, bool MX, bool XF>
-__global__ void __launch_bounds__(kRoundtripWarps * 32, kRoundtripCtas)
+__global__ void __launch_bounds__(kRoundtripWarps * 32, XF ? kRoundtripCtasF32 : kRoundtripCtas)
 roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap, TileLoop T) {
   constexpr int IN = XF ? 8192 : 4096;
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  const WarpSmem ws = warp_smem<kRoundtripStages, IN>(smem_raw, warp);
-  const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
+  const WarpSmem ws = warp_smem<kRoundtripStages, IN, RoundtripXBytes<XF>::value>(smem_raw, warp);
+  const XposeHalf xa = xpose_half_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<XF ? 8 : 4>(&xmap, T, t, buf, bar); };
   InPipe<kRoundtripStages, IN> pipe{};
   pipe.start(ws.stage0, ws.bar0, warp_global<kRoundtripWarps>(), warp_count<kRoundtripWarps>(), T.tiles, lane,
@@ -1187,7 +1245,7 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       rows_bfly(v, 1);
       rows_bfly(v, 2);
       staging_free(lane);
-      transpose<true>(v, xa);
+      transpose_half<true>(v, xa);
       rows_bfly(v, 1);
       rows_bfly(v, 2);
       if (MX) {
@@ -1200,7 +1258,7 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       dequantize(q.code, q.S, v, T.negzero);
       rows_bfly(v, 2);
       rows_bfly(v, 1);
-      transpose<false>(v, xa);
+      transpose_half<false>(v, xa);
       rows_bfly(v, 2);
       rows_bfly(v, 1);
       level1_inv(v);
@@ -1569,6 +1627,13 @@ struct Launch {
 };
 
 // Persistent grid: as many CTAs as fit on all SMs at once, never more than the tiles need.
+// CTAs per SM cap for a grid of `warps`-warp CTAs over `tiles` tiles, `ctas` per SM at most
+// (0: as many as fit).
+int small_grid_cap(int64_t tiles, int warps, int ctas) {
+  const int sms = num_sms();
+  return sms > 0 && tiles < (int64_t)kSmallGridTiles * warps * ctas * sms ? kSmallGridCtas : 0;
+}
+
 template <typename K>
 fp4q_status plan(K kernel, int warps, int smem, int64_t tiles, Launch& L, int max_per_sm = 0) {
   const int sms = num_sms();
@@ -1708,7 +1773,8 @@ fp4q_status launch_compress(const void* x, int64_t n, void* payload, cudaStream_
     auto k = compress_kernel<G, F, MX, XF>;
     Launch L;
     fp4q_status st = plan(k, kCompressWarps,
-                          WarpSmemLayout<kCompressWarps, kCompressStages, XF ? 8192 : 4096>::kCtaBytes, T.tiles, L);
+                          WarpSmemLayout<kCompressWarps, kCompressStages, XF ? 8192 : 4096, kCompressXBytes>::kCtaBytes, T.tiles, L,
+                          small_grid_cap(T.tiles, kCompressWarps, kCompressCtas));
     if (st == FP4Q_OK) st = launch_pdl(k, L, kCompressWarps * 32, s, xm, P, T);
     if (st != FP4Q_OK) return st;
   }
@@ -1750,7 +1816,8 @@ fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) 
     auto k = roundtrip_kernel<G, F, MX, XF>;
     Launch L;
     fp4q_status st = plan(k, kRoundtripWarps,
-                          WarpSmemLayout<kRoundtripWarps, kRoundtripStages, XF ? 8192 : 4096>::kCtaBytes, T.tiles, L);
+                          WarpSmemLayout<kRoundtripWarps, kRoundtripStages, XF ? 8192 : 4096, RoundtripXBytes<XF>::value>::kCtaBytes,
+                          T.tiles, L, XF ? 0 : small_grid_cap(T.tiles, kRoundtripWarps, kRoundtripCtas));
     if (st == FP4Q_OK) st = launch_pdl(k, L, kRoundtripWarps * 32, s, xm, ym, T);
     if (st != FP4Q_OK) return st;
   }
@@ -1777,8 +1844,8 @@ fp4q_status launch_compress_2d(const void* x, int64_t rows, int64_t cols, int64_
   if (!rows_map(&xm, x, rows, cols, ld, false)) return FP4Q_ERR_CUDA;
   auto k = compress_kernel<G, F, MX, false>;
   Launch L;
-  fp4q_status st = plan(k, kCompressWarps, WarpSmemLayout<kCompressWarps, kCompressStages, 4096>::kCtaBytes,
-                        T.tiles, L);
+  fp4q_status st = plan(k, kCompressWarps, WarpSmemLayout<kCompressWarps, kCompressStages, 4096, kCompressXBytes>::kCtaBytes,
+                        T.tiles, L, small_grid_cap(T.tiles, kCompressWarps, kCompressCtas));
   if (st != FP4Q_OK) return st;
   return launch_pdl(k, L, kCompressWarps * 32, s, xm, payload_of(payload, rows * cols, G, MX), T);
 }
@@ -1808,8 +1875,8 @@ fp4q_status launch_roundtrip_2d(const void* x, int64_t rows, int64_t cols, int64
   if (!rows_map(&xm, x, rows, cols, ldx, false) || !rows_map(&ym, y, rows, cols, ldy, false)) return FP4Q_ERR_CUDA;
   auto k = roundtrip_kernel<G, F, MX, false>;
   Launch L;
-  fp4q_status st = plan(k, kRoundtripWarps, WarpSmemLayout<kRoundtripWarps, kRoundtripStages, 4096>::kCtaBytes,
-                        T.tiles, L);
+  fp4q_status st = plan(k, kRoundtripWarps, WarpSmemLayout<kRoundtripWarps, kRoundtripStages, 4096, RoundtripXBytes<false>::value>::kCtaBytes,
+                        T.tiles, L, small_grid_cap(T.tiles, kRoundtripWarps, kRoundtripCtas));
   if (st != FP4Q_OK) return st;
   return launch_pdl(k, L, kRoundtripWarps * 32, s, xm, ym, T);
 }
