@@ -1020,66 +1020,72 @@ struct TileLoop {
 };
 
 // TMA traffic of one tile of a data tensor (x, y or dst) with LPB 128-byte lines per block
-// (4 for BF16, 8 for FP32). Contiguous data is a 2-D map of lines and a tile is one box;
-// a strided 2-D tensor is a 3-D map {line, line in row, row} and a tile is one box when rows
-// hold whole tiles (tpr), else one box per existing block (blocks never straddle rows: cols
-// is a multiple of 256). Each block lands at the same shared-memory offset either way, so
-// the swizzled tile layout is unchanged.
-template <int LPB>
-__device__ __forceinline__ void tile_load(const CUtensorMap* map, const TileLoop& T, int64_t t, uint32_t buf,
-                                          uint32_t bar) {
-  constexpr uint32_t BPB = 128u * LPB;
-  if (T.bpr == 0) {
-    mbar_expect_tx(bar, kTileBlocks * BPB);
-    tma_load_2d(buf, map, 0, (int32_t)(t * kTileBlocks * LPB), bar);
-    return;
-  }
-  if (T.tpr) {
-    const int64_t row = t / T.tpr;
-    mbar_expect_tx(bar, kTileBlocks * BPB);
-    tma_load_3d(buf, map, 0, (int32_t)((t - row * T.tpr) * kTileBlocks * LPB), (int32_t)row, bar);
-    return;
-  }
-  const int64_t gb0 = t * kTileBlocks;
-  const int nv = (int)(T.nb - gb0 < kTileBlocks ? T.nb - gb0 : kTileBlocks);
-  mbar_expect_tx(bar, (uint32_t)nv * BPB);
-  int32_t row = (int32_t)(gb0 / T.bpr);
-  int32_t line = (int32_t)((gb0 - (int64_t)row * T.bpr) * LPB);
-  const int32_t row_lines = (int32_t)(T.bpr * LPB);
-  for (int b = 0; b < nv; ++b) {
-    tma_load_3d(buf + (uint32_t)b * BPB, map, 0, line, row, bar);
-    line += LPB;
-    if (line == row_lines) {
-      line = 0;
-      ++row;
-    }
+// (4 for BF16, 8 for FP32); every lane of the warp calls these. Tile and block indices fit in
+// 32 bits (n < 2^37: fewer than 2^29 blocks), so the row divisions are 32-bit. Contiguous data is a 2-D map
+// of lines and a tile is one box, issued by lane 0. A strided 2-D tensor is a 3-D map
+// {line, line in row, row}: a tile is one box when rows hold whole tiles (tpr), else one box
+// per existing block (blocks never straddle rows: cols is a multiple of 256), lane b issuing
+// block b's box after lane 0 has armed the barrier for all of them. Each block lands at the
+// same shared-memory offset either way, so the swizzled tile layout is unchanged.
+// One box per existing block of tile t (nb blocks in all, bpr per row, lpb lines per block).
+// Kept out of line: it runs only for strided tensors whose rows do not hold whole tiles, and
+// inlined its registers weighed on every kernel's common path.
+__device__ __noinline__ void blocks_load(const CUtensorMap* map, uint32_t nb, uint32_t bpr, uint32_t t, uint32_t buf,
+                                         uint32_t bar, int lane, uint32_t lpb) {
+  const uint32_t gb0 = t * kTileBlocks, bpb = 128u * lpb;
+  const int nv = (int)(nb - gb0 < (uint32_t)kTileBlocks ? nb - gb0 : (uint32_t)kTileBlocks);
+  if (lane == 0) mbar_expect_tx(bar, (uint32_t)nv * bpb);
+  __syncwarp();
+  if (lane < nv) {
+    const uint32_t gb = gb0 + (uint32_t)lane, row = gb / bpr;
+    tma_load_3d(buf + (uint32_t)lane * bpb, map, 0, (int32_t)((gb - row * bpr) * lpb), (int32_t)row, bar);
   }
 }
+__device__ __noinline__ void blocks_store(const CUtensorMap* map, uint32_t nb, uint32_t bpr, uint32_t t, uint32_t src,
+                                          int lane, uint32_t lpb) {
+  const uint32_t gb0 = t * kTileBlocks, bpb = 128u * lpb;
+  const int nv = (int)(nb - gb0 < (uint32_t)kTileBlocks ? nb - gb0 : (uint32_t)kTileBlocks);
+  if (lane < nv) {
+    const uint32_t gb = gb0 + (uint32_t)lane, row = gb / bpr;
+    tma_store_3d(map, 0, (int32_t)((gb - row * bpr) * lpb), (int32_t)row, src + (uint32_t)lane * bpb);
+    bulk_commit();
+  }
+}
+
 template <int LPB>
-__device__ __forceinline__ void tile_store(const CUtensorMap* map, const TileLoop& T, int64_t t, uint32_t src) {
+__device__ __forceinline__ void tile_load(const CUtensorMap* map, const TileLoop& T, int64_t t, uint32_t buf,
+                                          uint32_t bar, int lane) {
   constexpr uint32_t BPB = 128u * LPB;
-  if (T.bpr == 0) {
-    tma_store_2d(map, 0, (int32_t)(t * kTileBlocks * LPB), src);
-    return;
-  }
-  if (T.tpr) {
-    const int64_t row = t / T.tpr;
-    tma_store_3d(map, 0, (int32_t)((t - row * T.tpr) * kTileBlocks * LPB), (int32_t)row, src);
-    return;
-  }
-  const int64_t gb0 = t * kTileBlocks;
-  const int nv = (int)(T.nb - gb0 < kTileBlocks ? T.nb - gb0 : kTileBlocks);
-  int32_t row = (int32_t)(gb0 / T.bpr);
-  int32_t line = (int32_t)((gb0 - (int64_t)row * T.bpr) * LPB);
-  const int32_t row_lines = (int32_t)(T.bpr * LPB);
-  for (int b = 0; b < nv; ++b) {
-    tma_store_3d(map, 0, line, row, src + (uint32_t)b * BPB);
-    line += LPB;
-    if (line == row_lines) {
-      line = 0;
-      ++row;
+  if (T.bpr == 0 || T.tpr) {
+    if (lane != 0) return;
+    mbar_expect_tx(bar, kTileBlocks * BPB);
+    if (T.bpr == 0) {
+      tma_load_2d(buf, map, 0, (int32_t)(t * kTileBlocks * LPB), bar);
+    } else {
+      const uint32_t row = (uint32_t)t / (uint32_t)T.tpr;
+      tma_load_3d(buf, map, 0, (int32_t)(((uint32_t)t - row * (uint32_t)T.tpr) * kTileBlocks * LPB), (int32_t)row, bar);
     }
+    return;
   }
+  blocks_load(map, (uint32_t)T.nb, (uint32_t)T.bpr, (uint32_t)t, buf, bar, lane, LPB);
+}
+// Store tile t from the staging buffer; each issuing lane commits its own bulk group.
+template <int LPB>
+__device__ __forceinline__ void tile_store(const CUtensorMap* map, const TileLoop& T, int64_t t, uint32_t src,
+                                           int lane) {
+  constexpr uint32_t BPB = 128u * LPB;
+  if (T.bpr == 0 || T.tpr) {
+    if (lane != 0) return;
+    if (T.bpr == 0) {
+      tma_store_2d(map, 0, (int32_t)(t * kTileBlocks * LPB), src);
+    } else {
+      const uint32_t row = (uint32_t)t / (uint32_t)T.tpr;
+      tma_store_3d(map, 0, (int32_t)(((uint32_t)t - row * (uint32_t)T.tpr) * kTileBlocks * LPB), (int32_t)row, src);
+    }
+    bulk_commit();
+    return;
+  }
+  blocks_store(map, (uint32_t)T.nb, (uint32_t)T.bpr, (uint32_t)t, src, lane, LPB);
 }
 
 // Zero a CTA's tile counter before any warp claims from it.
@@ -1095,9 +1101,10 @@ __device__ __forceinline__ int64_t warp_global() {
 template <int WARPS>
 __device__ __forceinline__ int64_t warp_count() { return (int64_t)gridDim.x * WARPS; }
 
-// Lane 0 of the warp waits until its last TMA store has finished reading the staging buffer.
-__device__ __forceinline__ void staging_free(int lane) {
-  if (lane == 0) bulk_wait_read_all();
+// Wait until the warp's TMA stores have finished reading the staging buffer (every lane waits
+// for the bulk groups it committed itself).
+__device__ __forceinline__ void staging_free() {
+  bulk_wait_read_all();
   __syncwarp();
 }
 // Publish the staging buffer (written with st.shared) to the TMA store of tile t.
@@ -1106,10 +1113,7 @@ __device__ __forceinline__ void staging_store(const CUtensorMap* map, const Tile
                                               int lane) {
   fence_proxy_async();
   __syncwarp();
-  if (lane == 0) {
-    tile_store<LPB>(map, T, t, xbuf);
-    bulk_commit();
-  }
+  tile_store<LPB>(map, T, t, xbuf, lane);
 }
 
 // K1: compress. x (bfloat16, n) -> payload. Input tiles arrive by TMA.
@@ -1124,8 +1128,8 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kCompressStages, IN, kCompressXBytes>(smem_raw, warp);
   const XposeHalf xa = xpose_half_addr(ws.xbuf, blk, l4);
-  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<XF ? 8 : 4>(&xmap, T, t, buf, bar); };
-  InPipe<kCompressStages, IN> pipe{};
+  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<XF ? 8 : 4>(&xmap, T, t, buf, bar, lane); };
+  InPipe<kCompressStages, IN, true> pipe{};
   pipe.start(ws.stage0, ws.bar0, warp_global<kCompressWarps>(), warp_count<kCompressWarps>(), T.tiles, lane, issue);
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
     const int64_t gb = t * kTileBlocks + blk;
@@ -1171,8 +1175,8 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kDecompressStages, BETA ? TB : 0>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
-  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<LPB>(&dmap, T, t, buf, bar); };
-  InPipe<kDecompressStages, TB> pipe{};
+  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<LPB>(&dmap, T, t, buf, bar, lane); };
+  InPipe<kDecompressStages, TB, true> pipe{};
   const int64_t t0 = warp_global<kDecompressWarps>(), W = warp_count<kDecompressWarps>();
   if (BETA) pipe.start(ws.stage0, ws.bar0, t0, W, T.tiles, lane, issue);
   PayRaw cur, nxt;
@@ -1186,7 +1190,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
     if (FWHT) scale_by_16th(S);
     Rows v;
     dequantize(cur.code, S, v, T.negzero);
-    staging_free(lane);
+    staging_free();
     if (FWHT) {
       rows_bfly(v, 2);             // h = 128
       rows_bfly(v, 1);             // h = 64
@@ -1215,7 +1219,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
     }
     cur.sb = nxt.sb;
   }
-  if (lane == 0) bulk_wait_all();
+  bulk_wait_all();
 }
 
 // K3: fused roundtrip. x (bfloat16) -> y = bf16(decode(compress(x))), no payload.
@@ -1230,8 +1234,8 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
   const WarpSmem ws = warp_smem<kRoundtripStages, IN, RoundtripXBytes<XF>::value>(smem_raw, warp);
   const XposeHalf xa = xpose_half_addr(ws.xbuf, blk, l4);
-  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<XF ? 8 : 4>(&xmap, T, t, buf, bar); };
-  InPipe<kRoundtripStages, IN> pipe{};
+  auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<XF ? 8 : 4>(&xmap, T, t, buf, bar, lane); };
+  InPipe<kRoundtripStages, IN, true> pipe{};
   pipe.start(ws.stage0, ws.bar0, warp_global<kRoundtripWarps>(), warp_count<kRoundtripWarps>(), T.tiles, lane,
              issue);
   for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
@@ -1244,7 +1248,7 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       level1_fwd_from2(v);
       rows_bfly(v, 1);
       rows_bfly(v, 2);
-      staging_free(lane);
+      staging_free();
       transpose_half<true>(v, xa);
       rows_bfly(v, 1);
       rows_bfly(v, 2);
@@ -1265,12 +1269,12 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     } else {
       if (MX) quantize_mx<false>(v, q); else quantize<G, false, false>(v, q);
       dequantize(q.code, q.S, v, T.negzero);
-      staging_free(lane);
+      staging_free();
     }
     if (XF) tile_write_f32(ws.xbuf, blk, l4, v); else tile_write_bf16(ws.xbuf, blk, l4, v);
     staging_store<XF ? 8 : 4>(&ymap, T, t, ws.xbuf, lane);
   }
-  if (lane == 0) bulk_wait_all();
+  bulk_wait_all();
 }
 
 // K4: emulated R-way reduce. R payloads -> transform-domain FP32 sum in rank order ->

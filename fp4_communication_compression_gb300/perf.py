@@ -7,7 +7,9 @@ Each kernel is timed alone with CUDA events on the launching stream, after an L2
 (a write of a buffer larger than L2 followed by a read of another one), and reported as
 algorithmic GB/s (the bytes the kernel must move, G = 16; the *_mx kernels use the E8M0
 variant, group 32; compress_f32 / roundtrip_f32 take FP32 input; compress_2d reads a strided
-[n/4096, 4096] view of an [n/4096, 8192] matrix) and as a fraction of the measured
+[n/4096, 4096] view of an [n/4096, 8192] matrix, one TMA box per tile; the *_2d_blocks
+kernels read (and roundtrip writes) [n/1024, 1024] views of [n/1024, 2048] matrices, one
+box per block) and as a fraction of the measured
 HBM copy bandwidth in MEASURED_PEAKS.json when that file is present. Inputs are N(0,1)
 bfloat16 tensors made on the device (timing only; parity is the tests' business).
 """
@@ -41,6 +43,8 @@ ALG_BYTES = {
     "compress_f32": 4 + PAYLOAD,
     "roundtrip_f32": 8.0,
     "compress_2d": 2 + PAYLOAD,
+    "compress_2d_blocks": 2 + PAYLOAD,
+    "roundtrip_2d_blocks": 4.0,
 }
 
 
@@ -95,6 +99,12 @@ def main():
         yf = torch.empty_like(xf) if f32 else None
         # rows of 4096 elements every 8192: the left half of a twice wider matrix
         wide = torch.empty(n // 4096, 8192, dtype=torch.bfloat16, device=dev) if "compress_2d" in args.kernels else None
+        # rows of 1024 elements every 2048 (4 blocks per row: one TMA box per block)
+        blocks = any(k.endswith("_2d_blocks") for k in args.kernels)
+        nar = torch.empty(n // 1024, 2048, dtype=torch.bfloat16, device=dev) if blocks else None
+        nar_y = torch.empty(n // 1024, 2048, dtype=torch.bfloat16, device=dev) if blocks else None
+        if nar is not None:
+            nar[:, :1024] = x.view(-1, 1024)
         if wide is not None:
             wide[:, :4096] = x.view(-1, 4096)
         pm = [fq.compress(x * (r + 1), scales="e8m0") for r in range(4)] if mx else None
@@ -116,13 +126,15 @@ def main():
             "compress_f32": lambda: fq.compress(xf, payload=ps[0]),
             "roundtrip_f32": lambda: fq.roundtrip(xf, y=yf),
             "compress_2d": lambda: fq.compress(wide[:, :4096], payload=ps[0]),
+            "compress_2d_blocks": lambda: fq.compress(nar[:, :1024], payload=ps[0]),
+            "roundtrip_2d_blocks": lambda: fq.roundtrip(nar[:, :1024], y=nar_y[:, :1024]),
         }
         for k in args.kernels:
             t = timed(fns[k])
             gbs = ALG_BYTES[k] * n / t / 1e9
             print(json.dumps({"n": n, "kernel": k, "us": round(t * 1e6, 2), "alg_gbs": round(gbs, 1),
                               "frac_of_peak": None if not peak else round(gbs / peak, 4)}), flush=True)
-        del x, ps, d16, d32, y, out, pm, outm, xf, yf, wide
+        del x, ps, d16, d32, y, out, pm, outm, xf, yf, wide, nar, nar_y
 
 
 if __name__ == "__main__":
