@@ -24,13 +24,16 @@
 //
 // Data movement and scheduling. Each warp streams its tiles through its own TMA pipeline
 // (InPipe: mbarrier-tracked cp.async.bulk.tensor loads with bounded waits), and BF16 / FP32
-// outputs leave by TMA stores from a swizzled staging buffer. Tiles are assigned round robin
-// to the warps of the grid; large reduces instead run one CTA per SM whose warps claim tiles
-// from a shared-memory counter. Every kernel starts with griddepcontrol.wait and is launched
-// with programmatic stream serialisation, so back-to-back codec kernels overlap launch and
-// drain. The same kernels serve the E8M0 (microscaled) scales, FP32 input, strided 2-D
-// views (3-D tensor maps) and, through one-warp tail kernels, lengths that are not a
-// multiple of 256.
+// outputs leave by TMA stores from a swizzled staging buffer; where a tile needs one box per
+// block (strided rows that do not hold whole tiles) eight lanes issue them. Tiles are
+// assigned round robin to the warps of the grid; large reduces instead run one CTA per SM
+// whose warps claim tiles from a shared-memory counter. Every kernel starts with
+// griddepcontrol.wait and is launched with programmatic stream serialisation, so
+// back-to-back codec kernels overlap launch and drain; for that overlap every kernel asks for
+// the largest shared-memory carveout, and a cap on CTAs per SM is enforced by padding the
+// dynamic shared memory (plan). The same kernels serve the E8M0 (microscaled) scales, FP32
+// input, strided 2-D views (3-D tensor maps) and, through one-warp tail kernels, lengths that
+// are not a multiple of 256.
 //
 // Exactness. Every floating-point step is a separately rounded FP32 operation: the file is
 // built with -fmad=false, packed ops carry .rn, no operation is reassociated, and the scale
