@@ -54,6 +54,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <utility>
 
@@ -1076,7 +1077,6 @@ __device__ __forceinline__ void tile_load(const CUtensorMap* map, const TileLoop
 template <int LPB>
 __device__ __forceinline__ void tile_store(const CUtensorMap* map, const TileLoop& T, int64_t t, uint32_t src,
                                            int lane) {
-  constexpr uint32_t BPB = 128u * LPB;
   if (T.bpr == 0 || T.tpr) {
     if (lane != 0) return;
     if (T.bpr == 0) {
@@ -1582,17 +1582,19 @@ __global__ void selftest_wait_kernel(uint32_t polls) {
 
 // ------------------------------------------------------------------ host side
 
-int g_num_sms[64];
+// Per-device attribute caches: written once per device with the same value by whichever
+// thread gets there first (atomics, so concurrent first calls are well defined).
+std::atomic<int> g_num_sms[64];
 
 int num_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
-  if (g_num_sms[dev] == 0) {
-    int v = 0;
+  int v = g_num_sms[dev].load();
+  if (v == 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    g_num_sms[dev] = v;
+    g_num_sms[dev].store(v);
   }
-  return g_num_sms[dev];
+  return v;
 }
 
 // Resident CTAs per SM of a kernel instance on the current device, with its dynamic
@@ -1648,19 +1650,20 @@ int small_grid_cap(int64_t tiles, int warps, int ctas) {
 // Shared memory of one SM and the part of it reserved per CTA, on the current device
 // (queried once per device).
 bool smem_per_sm(int& total, int& reserved) {
-  static int g_total[64], g_reserved[64];
+  static std::atomic<int> g_total[64], g_reserved[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  if (g_total[dev] == 0) {
-    int t = 0, r = 0;
+  int t = g_total[dev].load();
+  int r = g_reserved[dev].load();
+  if (t == 0) {
     if (cudaDeviceGetAttribute(&t, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&r, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess || t <= 0)
       return false;
-    g_reserved[dev] = r;
-    g_total[dev] = t;
+    g_reserved[dev].store(r);   // before total: a reader that sees total also sees reserved
+    g_total[dev].store(t);
   }
-  total = g_total[dev];
-  reserved = g_reserved[dev];
+  total = t;
+  reserved = r;
   return true;
 }
 
