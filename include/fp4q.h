@@ -79,7 +79,10 @@
  * runtime call to report). Kernels are launched with programmatic stream serialisation:
  * a codec kernel may be scheduled while the previous kernel on the stream is finishing,
  * but it waits for that kernel to complete (and for its memory to be visible) before its
- * first global-memory access, so stream order is preserved exactly.
+ * first global-memory access, so stream order is preserved exactly. The first call of each
+ * kernel variant on a device sets that kernel's dynamic shared-memory limit and preferred
+ * shared-memory carveout (the largest) and queries its occupancy; the results are cached per
+ * kernel and device, and the library's own kernels are the only ones it configures.
  */
 #ifndef FP4Q_H
 #define FP4Q_H
