@@ -758,7 +758,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 
 constexpr int kTileLinesBF16 = 32;         // 128-byte lines per 8-block bf16 tile (4 KiB)
 constexpr int kTileLinesF32 = 64;          // 128-byte lines per 8-block f32 tile (8 KiB)
-constexpr int kXBufBytes = 8192;           // transpose buffer / output staging per warp
+constexpr int kXBufBytes = 8192;           // full-width transpose buffer / output staging per warp
 constexpr int kCompressXBytes = kTileBlocks * kXHalfBlockBytes;   // compress: half-width transpose
 // roundtrip: half-width transpose; the buffer also stages the output tile (8 KiB for FP32)
 template <bool XF>
