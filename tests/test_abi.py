@@ -27,6 +27,14 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(fp4q_[a-z_0-9]+)\s*\(", text)))
 
 
+def test_build_flags_keep_exact_arithmetic():
+    """Bit parity with the oracle needs every FP32 operation rounded on its own: the library
+    must be built without FMA contraction, for sm_103a only."""
+    assert "-fmad=false" in _lib.NVCC_FLAGS
+    assert not any("fast-math" in f or "ftz=true" in f for f in _lib.NVCC_FLAGS)
+    assert "arch=compute_103a,code=sm_103a" in _lib.NVCC_FLAGS
+
+
 def test_header_declares_the_binding_exports():
     assert declared_functions() == sorted(_lib.EXPORTS)
 
