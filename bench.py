@@ -234,7 +234,8 @@ def reference_arm(args, rank, world):
             "config": {"workload": WORKLOAD, "ranks": R_RANKS, "shape": [TOKENS, HIDDEN], "group": GROUP,
                        "block": 256, "fwht": FWHT},
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{steps} full steps (capped at 20 of the requested {args.steps})"},
+                             "sample": f"{steps} full step{'s' if steps > 1 else ''} of {WORKLOAD}" + (
+                                 f" (the requested {args.steps} capped at 20)" if args.steps > steps else "")},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
