@@ -15,6 +15,16 @@ and returns without synchronising. The codec itself runs only in the sm_103a ker
 32); ``scales="e8m0"`` the power-of-two scale per group of 32 with no block scale. Every
 call on one payload must use the same group, fwht and scales.
 
+Every buffer a caller passes in is checked on the host before anything is launched (the C
+ABI sees only pointers and cannot know how long a buffer is): payloads must be contiguous
+uint8 CUDA tensors of at least ``payload_bytes(n, ...)`` bytes on the data tensor's device,
+data tensors CUDA tensors of the right dtype and size; a wrong buffer raises ``ValueError``.
+
+A return without an exception means the kernels were launched, not that they completed: a
+kernel whose bounded wait on a copy gives up returns early and sets the device fault word.
+``check=True`` synchronises the device after the call and raises ``Fp4qFault`` if that word
+is set (the word is cleared when read this way).
+
 Method: "FP4Quant: Efficient 4-Bit Communication Compression for Model-Parallel LLM
 Training" (abstract: micro-grouped dual-scale FP4 quantization, warp-cooperative FP4
 packing, hybrid two-level FWHT).
@@ -28,7 +38,17 @@ from ._lib import BF16, F32, Fp4qError, build  # noqa: F401
 
 __all__ = ["payload_bytes", "gscale_offset", "bscale_offset", "compress",
            "decompress_accumulate", "roundtrip", "reduce_requantize", "build", "Fp4qError",
-           "library_path", "fault_flags"]
+           "Fp4qFault", "library_path", "fault_flags"]
+
+
+class Fp4qFault(RuntimeError):
+    """The device fault word was set: a kernel gave up a bounded wait and returned early,
+    so the outputs of the calls since the word was last cleared are incomplete."""
+
+    def __init__(self, flags: int):
+        super().__init__(f"fp4q device fault word 0x{flags:x}: a kernel gave up waiting for a copy "
+                         "and returned early (outputs incomplete)")
+        self.flags = flags
 
 
 def library_path() -> str:
@@ -43,11 +63,51 @@ def _stream(stream, device):
 
 
 def _dev(t, name):
-    if not t.is_cuda:
+    if not getattr(t, "is_cuda", False):
         raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _buffer(t, name, nbytes, device):
+    """A payload buffer: a contiguous uint8 CUDA tensor on `device` of at least nbytes bytes
+    (the kernels read or write exactly payload_bytes(n) bytes from its start)."""
+    import torch
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.uint8:
+        raise ValueError(f"{name} must be uint8 (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the data tensor on {device}")
+    if t.numel() < nbytes:
+        raise ValueError(f"{name} holds {t.numel()} bytes, the payload needs {nbytes}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need_bytes(n, group, fwht, scales) -> int:
+    nb = payload_bytes(n, group, fwht, scales)
+    if nb == 0:
+        raise ValueError(f"invalid size {n} or parameters (group={group}, fwht={fwht}, scales={scales!r})")
+    return nb
+
+
+def _cuda_data(t, name):
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _fault_check(device, check):
+    if not check:
+        return
+    import torch
+    torch.cuda.synchronize(device)
+    with torch.cuda.device(device):
+        flags = fault_flags(clear=True)
+    if flags:
+        raise Fp4qFault(flags)
 
 
 def _strided_2d(t) -> bool:
@@ -71,9 +131,11 @@ def bscale_offset(n: int, group: int | None = None, fwht: int = 1, scales: str =
     return int(_lib.lib().fp4q_bscale_offset(int(n), ctypes.byref(p)))
 
 
-def compress(x, payload=None, group: int | None = None, fwht: int = 1, stream=None, scales: str = "dual"):
+def compress(x, payload=None, group: int | None = None, fwht: int = 1, stream=None, scales: str = "dual",
+             check: bool = False):
     """bfloat16 or float32 CUDA tensor -> uint8 payload tensor (allocated by torch if not given)."""
     import torch
+    _cuda_data(x, "x")
     if x.dtype == torch.bfloat16:
         fn, name = _lib.lib().fp4q_compress, "fp4q_compress"
     elif x.dtype == torch.float32:
@@ -83,26 +145,27 @@ def compress(x, payload=None, group: int | None = None, fwht: int = 1, stream=No
     n = x.numel()
     if _strided_2d(x) and x.dtype != torch.bfloat16:
         raise ValueError("strided 2-D input must be bfloat16")
+    nb = _need_bytes(n, group, fwht, scales)
     if payload is None:
-        nb = payload_bytes(n, group, fwht, scales)
-        if nb == 0:
-            raise ValueError(f"invalid size {n} or parameters")
         payload = torch.empty(nb, dtype=torch.uint8, device=x.device)
+    pp = _buffer(payload, "payload", nb, x.device)
     p = _lib.params(group, fwht, scales=scales)
     if _strided_2d(x):
         st = _lib.lib().fp4q_compress_2d(ctypes.c_void_p(x.data_ptr()), x.size(0), x.size(1), x.stride(0),
-                                         _dev(payload, "payload"), ctypes.byref(p), _stream(stream, x.device))
+                                         pp, ctypes.byref(p), _stream(stream, x.device))
         _lib.check("fp4q_compress_2d", st)
-        return payload
-    st = fn(_dev(x, "x"), n, _dev(payload, "payload"), ctypes.byref(p), _stream(stream, x.device))
-    _lib.check(name, st)
+    else:
+        st = fn(_dev(x, "x"), n, pp, ctypes.byref(p), _stream(stream, x.device))
+        _lib.check(name, st)
+    _fault_check(x.device, check)
     return payload
 
 
 def decompress_accumulate(payload, n: int, dst, beta: int = 1, group: int | None = None, fwht: int = 1,
-                          stream=None, scales: str = "dual"):
+                          stream=None, scales: str = "dual", check: bool = False):
     """dst (bfloat16 or float32 CUDA tensor of n elements) = beta ? dst + x^ : x^."""
     import torch
+    _cuda_data(dst, "dst")
     if dst.dtype == torch.bfloat16:
         dt = BF16
     elif dst.dtype == torch.float32:
@@ -111,24 +174,27 @@ def decompress_accumulate(payload, n: int, dst, beta: int = 1, group: int | None
         raise TypeError("dst must be bfloat16 or float32")
     if dst.numel() != n:
         raise ValueError("dst must have n elements")
+    pp = _buffer(payload, "payload", _need_bytes(n, group, fwht, scales), dst.device)
     p = _lib.params(group, fwht, scales=scales)
     if _strided_2d(dst):
-        st = _lib.lib().fp4q_decompress_accumulate_2d(_dev(payload, "payload"), dst.size(0), dst.size(1),
+        st = _lib.lib().fp4q_decompress_accumulate_2d(pp, dst.size(0), dst.size(1),
                                                       ctypes.c_void_p(dst.data_ptr()), dst.stride(0), dt,
                                                       int(beta), ctypes.byref(p), _stream(stream, dst.device))
         _lib.check("fp4q_decompress_accumulate_2d", st)
-        return dst
-    st = _lib.lib().fp4q_decompress_accumulate(_dev(payload, "payload"), int(n), _dev(dst, "dst"),
-                                               dt, int(beta), ctypes.byref(p),
-                                               _stream(stream, dst.device))
-    _lib.check("fp4q_decompress_accumulate", st)
+    else:
+        st = _lib.lib().fp4q_decompress_accumulate(pp, int(n), _dev(dst, "dst"), dt, int(beta), ctypes.byref(p),
+                                                   _stream(stream, dst.device))
+        _lib.check("fp4q_decompress_accumulate", st)
+    _fault_check(dst.device, check)
     return dst
 
 
-def roundtrip(x, y=None, group: int | None = None, fwht: int = 1, stream=None, scales: str = "dual"):
+def roundtrip(x, y=None, group: int | None = None, fwht: int = 1, stream=None, scales: str = "dual",
+              check: bool = False):
     """y = decode(compress(x)) in one kernel, no payload written; bfloat16 in and out, or
     float32 in and out (no bfloat16 rounding)."""
     import torch
+    _cuda_data(x, "x")
     if x.dtype == torch.bfloat16:
         fn, name = _lib.lib().fp4q_roundtrip, "fp4q_roundtrip"
     elif x.dtype == torch.float32:
@@ -137,8 +203,11 @@ def roundtrip(x, y=None, group: int | None = None, fwht: int = 1, stream=None, s
         raise TypeError("x must be bfloat16 or float32")
     if y is None:
         y = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    _cuda_data(y, "y")
     if y.dtype != x.dtype or y.numel() != x.numel():
         raise ValueError("y must match x in dtype and size")
+    if y.device != x.device:
+        raise ValueError(f"y is on {y.device}, x on {x.device}")
     p = _lib.params(group, fwht, scales=scales)
     if _strided_2d(x) or _strided_2d(y):
         if x.dtype != torch.bfloat16 or x.dim() != 2 or y.shape != x.shape:
@@ -147,26 +216,32 @@ def roundtrip(x, y=None, group: int | None = None, fwht: int = 1, stream=None, s
                                           ctypes.c_void_p(y.data_ptr()), y.stride(0), ctypes.byref(p),
                                           _stream(stream, x.device))
         _lib.check("fp4q_roundtrip_2d", st)
-        return y
-    st = fn(_dev(x, "x"), x.numel(), _dev(y, "y"), ctypes.byref(p), _stream(stream, x.device))
-    _lib.check(name, st)
+    else:
+        st = fn(_dev(x, "x"), x.numel(), _dev(y, "y"), ctypes.byref(p), _stream(stream, x.device))
+        _lib.check(name, st)
+    _fault_check(x.device, check)
     return y
 
 
 def reduce_requantize(payloads, n: int, out=None, group: int | None = None, fwht: int = 1, stream=None,
-                      scales: str = "dual"):
+                      scales: str = "dual", check: bool = False):
     """R payloads (uint8 CUDA tensors, same n and params) -> requantised sum payload."""
     import torch
     R = len(payloads)
-    ptrs = (ctypes.c_void_p * max(R, 1))(*[_dev(p, "payload").value for p in payloads])
+    if R < 1:
+        raise ValueError("reduce_requantize needs at least one payload")
+    nb = _need_bytes(n, group, fwht, scales)
+    _cuda_data(payloads[0], "payloads[0]")
+    device = payloads[0].device
+    ptrs = (ctypes.c_void_p * R)(*[_buffer(p, f"payloads[{i}]", nb, device).value for i, p in enumerate(payloads)])
     if out is None:
-        out = torch.empty(payload_bytes(n, group, fwht, scales), dtype=torch.uint8,
-                          device=payloads[0].device)
+        out = torch.empty(nb, dtype=torch.uint8, device=device)
+    po = _buffer(out, "out", nb, device)
     p = _lib.params(group, fwht, scales=scales)
-    st = _lib.lib().fp4q_reduce_requantize(ctypes.cast(ptrs, ctypes.c_void_p), R, int(n),
-                                           _dev(out, "out"), ctypes.byref(p),
-                                           _stream(stream, out.device))
+    st = _lib.lib().fp4q_reduce_requantize(ctypes.cast(ptrs, ctypes.c_void_p), R, int(n), po, ctypes.byref(p),
+                                           _stream(stream, device))
     _lib.check("fp4q_reduce_requantize", st)
+    _fault_check(device, check)
     return out
 
 

@@ -71,12 +71,18 @@
  *
  * Preconditions on data (not checked): inputs finite and |x| < 2^120.
  *
- * Threading and ownership: the caller owns every buffer; the library keeps no per-call
- * state and allocates no device memory (its only device data is the 4-byte fault word read
- * by fp4q_fault_flags). All entry points are asynchronous on the given
- * stream and never synchronise. Argument errors are returned before anything is launched.
- * A failed launch returns FP4Q_ERR_CUDA (the CUDA error is left to the caller's next
- * runtime call to report). Kernels are launched with programmatic stream serialisation:
+ * Threading and ownership: the caller owns every buffer, and the library allocates no device
+ * memory. The library holds process-wide state of two kinds: a cache, per kernel variant
+ * and device, of the launch plan (shared-memory attributes set once, the occupancy query),
+ * guarded by a mutex; and one 4-byte fault word per device (a __device__ variable, read and
+ * cleared by fp4q_fault_flags). Nothing else persists between calls. All entry points are
+ * asynchronous on the given stream and never synchronise. Argument errors are returned
+ * before anything is launched. A failed launch returns FP4Q_ERR_CUDA (the CUDA error is left
+ * to the caller's next runtime call to report). FP4Q_OK means the kernels were launched, not
+ * that they completed: a kernel whose bounded wait on a copy gives up returns early with its
+ * outputs incomplete and records this in the fault word, which the caller must read (after
+ * synchronising) to know that every call since the word was cleared ran to completion.
+ * Kernels are launched with programmatic stream serialisation:
  * a codec kernel may be scheduled while the previous kernel on the stream is finishing,
  * but it waits for that kernel to complete (and for its memory to be visible) before its
  * first global-memory access, so stream order is preserved exactly. The first call of each
