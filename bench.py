@@ -1,25 +1,33 @@
 #!/usr/bin/env python
 """Benchmark of the FP4 communication codec's hot path on GB300.
 
-One step = one emulated R-rank compressed AllReduce of a tensor-parallel activation
-(workload: two [4096, 4096] bfloat16 partial sums drawn like the 4096 x 4096 TP activation
-of a 7B-class model, seeds 0 and 1): compress each rank's partial, fused
-decompress-sum-requantize of the R payloads, then decompress-accumulate the reduced payload
-into a bfloat16 residual stream. Every kernel of the path runs once per step (R compresses,
-one reduce, one decompress-accumulate).
+Headline workload (the largest single-GPU size of the size sweep): one 1-D bfloat16 tensor
+of n = 2^29 elements (1 GiB), N(0,1) with 0.1% of the entries x20 (seed 0). One step =
+compress it, then decompress-accumulate the payload (beta = 1) into a bfloat16 residual of
+the same size: the send and receive side of one compressed exchange. Every kernel of the
+step runs once per step; L2 is flushed between steps.
 
-Metric: GB/s of BF16 input (R * 2n bytes per step / step time), with each kernel's
-achieved algorithmic bandwidth against the measured HBM copy peak. The step time comes from
-CUDA events at step boundaries only (the kernels launch with programmatic stream
-serialisation, and an event between two kernels would stop that overlap); the per-kernel
-durations come from a second pass of the same steps with an event between kernels.
+Metric: GB/s of BF16 input (2n bytes per step / step time), with each kernel's achieved
+algorithmic bandwidth against the measured HBM copy peak. The step time comes from CUDA
+events at step boundaries only (the kernels launch with programmatic stream serialisation,
+and an event between two kernels would stop that overlap); the per-kernel durations come
+from a second pass of the same steps with an event between kernels.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+The same JSON line carries one record per workload ("configs"): the toy [8, 512] tensor
+with a 2-rank reduce, the [4096, 4096] TP activation, the emulated 4-rank reduce of
+4 x [8192, 4096] (plus R = 2 and R = 8 on the same payloads), the [16384, 4096] gradient at
+G = 16/32 with the transform on and off, and the size sweep 2^15 ... 2^29. Each kernel there
+is timed alone with cold inputs (L2 flushed before every launch; median of the launches)
+and carries its algorithmic GB/s, its fraction of the HBM peak, its code / value mismatches
+against the CPU oracle and the workload's relative L2 error.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-configs]
+    python bench.py --kernel compress --n 67108864 [--iters 3]     # one kernel alone
 
 Under torchrun (N > 1) every rank runs its own replica on its own GPU (weak scaling; the
 codec has no data-path collective), the timed region is bracketed by barriers and the
 slowest rank's time is reported. --impl reference times the CPU oracle (the plain scalar
-restatement used by the tests) on the same workload and metric.
+restatement used by the tests) on a bounded sample of the same workload and metric.
 """
 from __future__ import annotations
 
@@ -37,35 +45,77 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-R_RANKS = 2
-TOKENS, HIDDEN = 4096, 4096
+HEADLINE_N = 1 << 29
 GROUP, FWHT = 16, 1
-WORKLOAD = "tp_activation_4096x4096_allreduce_r2"
+WORKLOAD = "sweep_2p29_compress_decompress_accumulate"
 METRIC = "compress / decompress-accumulate GB/s of BF16 input"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 512 << 20
+L2_POLICY = (f"flushed between steps and before every per-config launch ({L2_FLUSH_BYTES >> 20} MiB write + "
+             f"{L2_FLUSH_BYTES >> 20} MiB read, outside the timed events); headline tensors are also larger than L2")
+REF_SAMPLE = 1 << 26                 # elements of each reference-arm step (a sample of the workload)
+CPU_SAMPLE = 1 << 24                 # elements of each cpu_baseline repetition
+TARGET_FRAC = 0.70
+TARGET_MIN_BYTES = 64 << 20          # the target applies to workloads of at least 64 MiB of BF16
 
-# algorithmic bytes per element (G = 16): what each kernel must move at minimum
-ALG_BYTES = {
-    "compress": 2 + 0.5 + 1 / 16 + 4 / 256,
-    "reduce": (R_RANKS + 1) * (0.5 + 1 / 16 + 4 / 256),
-    "decompress_accumulate": 0.5 + 1 / 16 + 4 / 256 + 4,
-}
+PAY16 = 0.5 + 1 / 16 + 4 / 256       # payload bytes per element, dual scales, G = 16
+PAY32 = 0.5 + 1 / 32 + 4 / 256       # dual scales, G = 32
+PAYMX = 0.5 + 1 / 32                 # E8M0 scales (group 32, no block scale)
 
 
-def parse():
+def payload_per_elem(group=16, scales="dual"):
+    return PAYMX if scales == "e8m0" else (PAY16 if group == 16 else PAY32)
+
+
+def alg_bytes(kernel: str, group=16, scales="dual") -> float:
+    """Bytes per element each kernel must move at minimum (reads + writes)."""
+    p = payload_per_elem(group, scales)
+    if kernel.startswith("reduce_r"):
+        return (int(kernel[len("reduce_r"):]) + 1) * p
+    table = {
+        "compress": 2 + p, "compress_f32": 4 + p, "compress_2d": 2 + p, "compress_2d_blocks": 2 + p,
+        "decompress_bf16_b1": p + 4, "decompress_bf16_b0": p + 2,
+        "decompress_f32_b1": p + 8, "decompress_f32_b0": p + 4,
+        "roundtrip": 4.0, "roundtrip_f32": 8.0, "roundtrip_2d_blocks": 4.0, "copy_bf16": 4.0,
+    }
+    return table[kernel]
+
+
+def bf16_in_bytes(kernel: str) -> float:
+    """BF16-input bytes per element the kernel stands for (R ranks for a reduce)."""
+    if kernel.startswith("reduce_r"):
+        return 2.0 * int(kernel[len("reduce_r"):])
+    return 2.0
+
+
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload records")
+    ap.add_argument("--config-iters", type=int, default=10, help="timed launches per per-config kernel")
+    ap.add_argument("--kernel", default=None, help="time one kernel alone and exit: compress, decompress_{bf16,f32}_b{0,1}, roundtrip, reduce_r<R>, "
+                    "copy_bf16, compress_f32, roundtrip_f32, compress_2d, compress_2d_blocks, roundtrip_2d_blocks; "
+                    "a _mx suffix selects the E8M0 scales")
+    ap.add_argument("--n", type=int, default=1 << 26, help="elements for --kernel")
+    ap.add_argument("--iters", type=int, default=30, help="timed launches for --kernel")
+    return ap.parse_args(argv)
 
 
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
         int(os.environ.get("LOCAL_RANK", 0))
+
+
+def bench_config(world: int) -> dict:
+    """The workload description both arms print (identical dicts)."""
+    return {"workload": WORKLOAD, "elements": HEADLINE_N, "shape": [HEADLINE_N], "input": "bf16",
+            "values": "N(0,1), 0.1% of entries x20, seed 0", "dst": "bf16 residual, beta=1",
+            "group": GROUP, "block": 256, "fwht": FWHT, "scales": "dual (E4M3 x FP32)",
+            "parallelism": f"replicas x{world}"}
 
 
 def measured_peak():
@@ -92,17 +142,23 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
+def ncu_traffic(kernel: str, n: int | None = None):
     """DRAM bytes per launch of a kernel from the committed ncu summary, or None when the
-    summary is missing or was taken on a different kernel source."""
+    summary is missing or was taken on a different kernel source. A summary stamped with
+    elements=m (a capture smaller than the bench launch) is scaled to n elements."""
     sha = kernel_source_sha()
-    for name in sorted(os.listdir(os.path.join(ROOT, "profiles"))) if os.path.isdir(os.path.join(ROOT, "profiles")) else []:
+    pdir = os.path.join(ROOT, "profiles")
+    for name in sorted(os.listdir(pdir)) if os.path.isdir(pdir) else []:
         if not name.endswith(".md"):
             continue
-        text = open(os.path.join(ROOT, "profiles", name)).read()
-        m = re.search(r"bench-traffic kernel=(\w+) source_sha256=(\w+) dram_bytes_per_launch=(\d+)", text)
+        text = open(os.path.join(pdir, name)).read()
+        m = re.search(r"bench-traffic kernel=(\w+) source_sha256=(\w+) dram_bytes_per_launch=(\d+)"
+                      r"(?: elements=(\d+))?", text)
         if m and m.group(1) == kernel and m.group(2) == sha:
-            return int(m.group(3))
+            b = int(m.group(3))
+            if m.group(4) and n:
+                b = int(round(b * n / int(m.group(4))))
+            return b
     return None
 
 
@@ -173,81 +229,382 @@ def job_gbs(bytes_per_rank_step: int, steps: int, world: int, max_ms: float) -> 
     return world * bytes_per_rank_step * steps / (max_ms * 1e-3) / 1e9
 
 
-def make_inputs():
+class FaultWordSet(RuntimeError):
+    pass
+
+
+def require_no_fault(fq, where: str) -> None:
+    """Refuse to report a number when a kernel gave up a bounded wait (its outputs, and so
+    its timing, would be those of an incomplete run). Reads and clears the device fault word
+    (this synchronises the device)."""
+    flags = fq.fault_flags(clear=True)
+    if flags:
+        raise FaultWordSet(f"device fault word 0x{flags:x} after {where}: a kernel returned early; "
+                           "no number is reported")
+
+
+def headline_inputs():
+    """The headline tensor and the residual it is accumulated into (bfloat16 bits)."""
     from fp4_communication_compression_gb300 import inputs
-    xs = [inputs.tp_activation(seed=r, tokens=TOKENS, hidden=HIDDEN) for r in range(R_RANKS)]
-    resid = inputs.tp_activation(seed=100, tokens=TOKENS, hidden=HIDDEN)
-    return xs, resid
+    return inputs.sweep(HEADLINE_N, seed=0), inputs.sweep(HEADLINE_N, seed=1)
 
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def oracle_step(xs, resid):
+def oracle_step(x, resid):
+    """compress + decompress-accumulate (beta = 1) of one sample on the CPU oracle."""
     import oracle
-    n = xs[0].size
-    pays = [oracle.compress(x.ravel(), GROUP, FWHT) for x in xs]
-    red = oracle.reduce_requantize(pays, n, GROUP)
-    return oracle.decompress_accumulate(red, n, resid.ravel().copy(), beta=1, group=GROUP, fwht=FWHT)
+    n = x.size
+    pay = oracle.compress(x, GROUP, FWHT)
+    return oracle.decompress_accumulate(pay, n, resid.copy(), beta=1, group=GROUP, fwht=FWHT)
 
 
-def time_oracle(xs, resid, min_seconds=10.0, max_reps=50):
+def oracle_sample(x, resid, elems):
+    return x[:elems], resid[:elems]
+
+
+def time_oracle(x, resid, elems=None, min_seconds=10.0, max_reps=200):
     import oracle
     oracle.set_threads(os.cpu_count() or 1)
     cores = oracle.max_threads()
-    n = xs[0].size
-    oracle_step(xs, resid)                         # build + warm
+    elems = min(elems or CPU_SAMPLE, x.size)
+    xs, rs = oracle_sample(x, resid, elems)
+    oracle_step(xs, rs)                              # build + warm
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle_step(xs, resid)
+        oracle_step(xs, rs)
         reps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds or reps >= max_reps:
             break
-    gbs = R_RANKS * 2 * n * reps / el / 1e9
+    gbs = 2 * elems * reps / el / 1e9
     return {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{reps} full steps of {WORKLOAD} ({R_RANKS} x {TOKENS}x{HIDDEN} bf16), "
-                      f"{el:.1f} s wall, OpenMP over 256-element blocks"}
+            "sample": f"{reps} steps (compress + decompress-accumulate) on the first {elems} elements "
+                      f"of the {WORKLOAD} tensor, {el:.1f} s wall, OpenMP over 256-element blocks"}
 
 
 def reference_arm(args, rank, world):
-    """CPU oracle as the reference implementation: same workload, metric and unit."""
+    """CPU oracle as the reference implementation: same workload description, metric and
+    unit; each step runs on a bounded sample (the first 2^26 elements) of the workload."""
     if rank != 0:
         return 0
-    xs, resid = make_inputs()
     import oracle
+    x, resid = headline_inputs()
     oracle.set_threads(os.cpu_count() or 1)
     cores = oracle.max_threads()
-    n = xs[0].size
+    elems = min(REF_SAMPLE, x.size)
+    xs, rs = oracle_sample(x, resid, elems)
     for _ in range(max(args.warmup, 0)):
-        oracle_step(xs, resid)
-    # each timed step is the full workload; keep the run to a few minutes
-    steps = max(1, min(args.steps, 20))
+        oracle_step(xs, rs)
+    steps = max(1, args.steps)
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle_step(xs, resid)
+        oracle_step(xs, rs)
     el = time.perf_counter() - t0
-    v = R_RANKS * 2 * n * steps / el / 1e9
+    v = 2 * elems * steps / el / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
             "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": WORKLOAD, "ranks": R_RANKS, "shape": [TOKENS, HIDDEN], "group": GROUP,
-                       "block": 256, "fwht": FWHT},
+            "data": "synthetic", "config": bench_config(world),
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{steps} full step{'s' if steps > 1 else ''} of {WORKLOAD}" + (
-                                 f" (the requested {args.steps} capped at 20)" if args.steps > steps else "")},
+                             "sample": f"each step: compress + decompress-accumulate of the first {elems} "
+                                       f"of the {HEADLINE_N} elements"},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
+# ------------------------------------------------------------------ GPU helpers
+
+class Timer:
+    """Per-launch device time of one kernel with cold inputs: L2 flushed before every
+    launch, events on the launching stream around the launch only."""
+
+    def __init__(self, torch, dev, stream):
+        self.torch, self.dev, self.stream = torch, dev, stream
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush(self):
+        # write a buffer larger than L2, then read another one: the reads evict the dirty
+        # lines, so their write-back is not charged to the next timed kernel
+        self.flush_buf.zero_()
+        self.clean.sum()
+
+    def median_ms(self, fn, iters, warm=3):
+        torch = self.torch
+        ts = []
+        for i in range(iters + warm):
+            self.flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            if i >= warm:
+                ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+
+def rel_l2(torch, got, ref):
+    """||got - ref|| / ||ref|| in float64 on the device (got, ref: any float dtypes)."""
+    g = got.double()
+    r = ref.double()
+    return float(torch.linalg.vector_norm(g - r) / torch.linalg.vector_norm(r))
+
+
+def kernel_record(name, n, ms, peak, group=16, scales="dual", **extra):
+    ab = alg_bytes(name, group, scales)
+    gbs = ab * n / (ms * 1e-3) / 1e9
+    rec = {"kernel": name, "n": n, "us": round(ms * 1e3, 2), "alg_bytes_per_elem": round(ab, 6),
+           "alg_gbs": round(gbs, 1), "bf16_in_gbs": round(bf16_in_bytes(name) * n / (ms * 1e-3) / 1e9, 1),
+           "frac_of_peak": round(gbs / peak, 4)}
+    rec.update(extra)
+    return rec
+
+
+def nibble_mismatches(a, b) -> int:
+    import numpy as np
+    d = np.bitwise_xor(np.asarray(a, np.uint8), np.asarray(b, np.uint8))
+    return int(np.count_nonzero(d & 15) + np.count_nonzero(d >> 4))
+
+
+def payload_mismatch(got, want, n, group=16, scales="dual"):
+    """(code mismatches, scale bytes that differ) of a GPU payload against the oracle's."""
+    import numpy as np
+    import oracle
+    g0 = oracle.gscale_offset(n, group, scales=scales)
+    return nibble_mismatches(got[:g0], want[:g0]), int(np.count_nonzero(got[g0:] != want[g0:]))
+
+
+# ------------------------------------------------------------------ per-config records
+
+def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
+    """One record per workload: every kernel timed alone with cold inputs, its parity against
+    the oracle (code / value mismatches) and the workload's relative L2 error."""
+    import numpy as np
+    import oracle
+    oracle.set_threads(os.cpu_count() or 1)
+    out = {}
+    gen = torch.Generator(device=dev)
+
+    def to_dev(bits):
+        return inputs.bits_to_torch(np.ascontiguousarray(bits).ravel(), dev)
+
+    def residual(n, seed):
+        gen.manual_seed(seed)
+        return torch.randn(n, generator=gen, device=dev).to(torch.bfloat16)
+
+    def codec_records(x_bits, tag, group=16, fwht=1, kernels=("compress", "decompress_bf16_b0",
+                                                              "decompress_bf16_b1", "roundtrip")):
+        """compress / decompress / roundtrip of one tensor: timings, parity, rel L2."""
+        x_bits = np.ascontiguousarray(x_bits).ravel()
+        n = x_bits.size
+        kw = dict(group=group, fwht=fwht)
+        x = to_dev(x_bits)
+        pay = fq.compress(x, **kw)
+        want = oracle.compress(x_bits, group, fwht)
+        got = pay.cpu().numpy()
+        cmis, smis = payload_mismatch(got, want, n, group)
+        recs = []
+        dst0 = residual(n, 1000 + n % 997)
+        dst = dst0.clone()
+        y = torch.empty_like(x)
+        for k in kernels:
+            if k == "compress":
+                ms = timer.median_ms(lambda: fq.compress(x, payload=pay, **kw), iters)
+                recs.append(kernel_record(k, n, ms, peak, group, code_mismatches=cmis, scale_byte_mismatches=smis))
+            elif k.startswith("decompress"):
+                beta = int(k[-1])
+                ms = timer.median_ms(lambda: fq.decompress_accumulate(pay, n, dst, beta=beta, **kw), iters)
+                dst.copy_(dst0)
+                fq.decompress_accumulate(pay, n, dst, beta=beta, **kw)
+                d0 = inputs.torch_to_bits(dst0)
+                ref = oracle.decompress_accumulate(got, n, d0, beta=beta, group=group, fwht=fwht)
+                vm = int(np.count_nonzero(inputs.torch_to_bits(dst) != ref))
+                recs.append(kernel_record(k, n, ms, peak, group, value_mismatches=vm))
+            elif k == "roundtrip":
+                ms = timer.median_ms(lambda: fq.roundtrip(x, y=y, **kw), iters)
+                # roundtrip = decode(compress(x)) with beta = 0: against the oracle's decode of
+                # its own payload
+                ref = oracle.decompress_accumulate(want, n, np.zeros(n, np.uint16), beta=0, group=group, fwht=fwht)
+                vm = int(np.count_nonzero(inputs.torch_to_bits(y) != ref))
+                recs.append(kernel_record(k, n, ms, peak, group, value_mismatches=vm))
+        fq.roundtrip(x, y=y, **kw)
+        err = rel_l2(torch, y.float(), x.float())
+        del x, pay, dst, dst0, y
+        return recs, err
+
+    # C1: toy [8, 512] with a 2-rank reduce (seeds 0 and 1)
+    xs = [inputs.toy(0).ravel(), inputs.toy(1).ravel()]
+    n = xs[0].size
+    recs, err = codec_records(xs[0], "toy", kernels=("compress", "decompress_bf16_b1", "roundtrip"))
+    pays = [fq.compress(to_dev(x)) for x in xs]
+    red = fq.reduce_requantize(pays, n)
+    ms = timer.median_ms(lambda: fq.reduce_requantize(pays, n, out=red), iters)
+    want = oracle.reduce_requantize([oracle.compress(x) for x in xs], n)
+    cm, sm = payload_mismatch(red.cpu().numpy(), want, n)
+    dec = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    fq.decompress_accumulate(red, n, dec, beta=0)
+    s = to_dev(xs[0]).double() + to_dev(xs[1]).double()
+    recs.append(kernel_record("reduce_r2", n, ms, peak, code_mismatches=cm, scale_byte_mismatches=sm))
+    out["C1_toy_8x512_r2"] = {"n": n, "bytes_bf16": 2 * n, "kernels": recs,
+                              "rel_l2_error": {"roundtrip": round(err, 6),
+                                               "reduce_r2": round(rel_l2(torch, dec.float(), s), 6)}}
+
+    # C2: TP activation [4096, 4096]
+    x = inputs.tp_activation()
+    recs, err = codec_records(x, "tp_act")
+    out["C2_tp_activation_4096x4096"] = {"n": x.size, "bytes_bf16": 2 * x.size, "kernels": recs,
+                                         "rel_l2_error": {"roundtrip": round(err, 6)}}
+
+    # C3: emulated 4-rank reduce, 4 x [8192, 4096] (seeds 1-4); R = 2 and 8 reuse the payloads
+    xs = [x.ravel() for x in inputs.reduce_ranks(4)]
+    n = xs[0].size
+    xt = [to_dev(x) for x in xs]
+    pays = [fq.compress(x) for x in xt]
+    wants = [oracle.compress(x) for x in xs]
+    cm = [payload_mismatch(p.cpu().numpy(), w, n) for p, w in zip(pays, wants)]
+    recs = [kernel_record("compress", n, timer.median_ms(lambda: fq.compress(xt[0], payload=pays[0]), iters), peak,
+                          code_mismatches=sum(c for c, _ in cm), scale_byte_mismatches=sum(s for _, s in cm),
+                          note="rank 0 timed; parity over all 4 ranks")]
+    red = torch.empty_like(pays[0])
+    dec = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    errs = {}
+    for R in (4, 2, 8):
+        sel = [i % 4 for i in range(R)]
+        ps = [pays[i] for i in sel]
+        ms = timer.median_ms(lambda: fq.reduce_requantize(ps, n, out=red), iters)
+        fq.reduce_requantize(ps, n, out=red)
+        want = oracle.reduce_requantize([wants[i] for i in sel], n)
+        c, s_ = payload_mismatch(red.cpu().numpy(), want, n)
+        recs.append(kernel_record(f"reduce_r{R}", n, ms, peak, code_mismatches=c, scale_byte_mismatches=s_))
+        if R == 4:
+            ms = timer.median_ms(lambda: fq.decompress_accumulate(red, n, dec, beta=0), iters)
+            fq.decompress_accumulate(red, n, dec, beta=0)
+            ref = oracle.decompress_accumulate(red.cpu().numpy(), n, np.zeros(n, np.uint16), beta=0)
+            recs.append(kernel_record("decompress_bf16_b0", n, ms, peak,
+                                      value_mismatches=int(np.count_nonzero(inputs.torch_to_bits(dec) != ref))))
+            ssum = sum(x.double() for x in xt)
+            errs["allreduce_r4"] = round(rel_l2(torch, dec.float(), ssum), 6)
+            del ssum
+    out["C3_reduce_4x8192x4096"] = {"n": n, "ranks": 4, "bytes_bf16": 2 * n, "kernels": recs,
+                                    "rel_l2_error": errs}
+    del xt, pays, red, dec
+
+    # C4: gradient [16384, 4096], G = 16 / 32 x transform on / off
+    x = inputs.gradient()
+    recs, errs = [], {}
+    for G in (16, 32):
+        for F in (1, 0):
+            r, e = codec_records(x, "grad", group=G, fwht=F,
+                                 kernels=("roundtrip",) if (G, F) != (16, 1) else
+                                 ("compress", "decompress_bf16_b1", "roundtrip"))
+            for rr in r:
+                rr.update(group=G, fwht=F)
+            recs += r
+            errs[f"roundtrip_g{G}_fwht{F}"] = round(e, 6)
+    out["C4_gradient_16384x4096"] = {"n": x.size, "bytes_bf16": 2 * x.size, "kernels": recs,
+                                     "rel_l2_error": errs}
+
+    # C5: size sweep 2^15 ... 2^29
+    for n in inputs.SWEEP_SIZES:
+        x = headline_x if (headline_x is not None and n == HEADLINE_N) else inputs.sweep(n)
+        recs, err = codec_records(x, "sweep")
+        out[f"C5_sweep_2p{n.bit_length() - 1}"] = {"n": n, "bytes_bf16": 2 * n, "kernels": recs,
+                                                  "rel_l2_error": {"roundtrip": round(err, 6)}}
+        torch.cuda.empty_cache()
+    return out
+
+
+def target_summary(configs):
+    """Every kernel record of a workload of at least 64 MiB of BF16 against the 70% target."""
+    rows, below = [], []
+    for name, c in configs.items():
+        if c["bytes_bf16"] < TARGET_MIN_BYTES:
+            continue
+        for k in c["kernels"]:
+            tag = f"{name}:{k['kernel']}" + (f"_g{k['group']}_fwht{k['fwht']}" if "group" in k else "")
+            rows.append(k["frac_of_peak"])
+            if k["frac_of_peak"] < TARGET_FRAC:
+                below.append({tag: k["frac_of_peak"]})
+    return {"target_frac": TARGET_FRAC, "records": len(rows), "met": len(rows) - len(below), "below": below,
+            "min_frac": min(rows) if rows else None}
+
+
+def parity_summary(configs):
+    tot = {"code_mismatches": 0, "scale_byte_mismatches": 0, "value_mismatches": 0}
+    for c in configs.values():
+        for k in c["kernels"]:
+            for key in tot:
+                tot[key] += int(k.get(key, 0))
+    return tot
+
+
+# ------------------------------------------------------------------ one kernel alone
+
+def kernel_mode(args):
+    """Time one kernel alone (L2 flushed before every launch) and print one JSON line; the
+    command the ncu summaries in profiles/ are taken on."""
+    import torch
+    import fp4_communication_compression_gb300 as fq
+    from fp4_communication_compression_gb300 import inputs
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    fq.build()
+    n, k = args.n, args.kernel
+    stream = torch.cuda.current_stream(dev)
+    timer = Timer(torch, dev, stream)
+    x = inputs.bits_to_torch(inputs.sweep(n), dev)
+    sc = "e8m0" if "_mx" in k else "dual"
+    base = k.replace("_mx", "")
+    R = int(base[len("reduce_r"):]) if base.startswith("reduce_r") else 0
+    pays = [fq.compress(x * (r + 1), scales=sc) for r in range(max(R, 1))]
+    out = torch.empty_like(pays[0])
+    d16 = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    d32 = torch.zeros(n, dtype=torch.float32, device=dev) if "f32" in base else None
+    y = torch.empty_like(x)
+    xf = x.float() if base in ("compress_f32", "roundtrip_f32") else None
+    yf = torch.empty_like(xf) if xf is not None else None
+    wide = nar = nar_y = None
+    if base == "compress_2d":            # rows of 4096 elements every 8192
+        wide = torch.empty(n // 4096, 8192, dtype=torch.bfloat16, device=dev)
+        wide[:, :4096] = x.view(-1, 4096)
+    if base.endswith("_2d_blocks"):      # rows of 1024 elements every 2048: one TMA box per block
+        nar = torch.empty(n // 1024, 2048, dtype=torch.bfloat16, device=dev)
+        nar_y = torch.empty_like(nar)
+        nar[:, :1024] = x.view(-1, 1024)
+    fns = {
+        "compress": lambda: fq.compress(x, payload=pays[0], scales=sc),
+        "decompress_bf16_b1": lambda: fq.decompress_accumulate(pays[0], n, d16, beta=1, scales=sc),
+        "decompress_bf16_b0": lambda: fq.decompress_accumulate(pays[0], n, d16, beta=0, scales=sc),
+        "decompress_f32_b1": lambda: fq.decompress_accumulate(pays[0], n, d32, beta=1, scales=sc),
+        "decompress_f32_b0": lambda: fq.decompress_accumulate(pays[0], n, d32, beta=0, scales=sc),
+        "roundtrip": lambda: fq.roundtrip(x, y=y, scales=sc),
+        "copy_bf16": lambda: y.copy_(x),
+        "compress_f32": lambda: fq.compress(xf, payload=pays[0]),
+        "roundtrip_f32": lambda: fq.roundtrip(xf, y=yf),
+        "compress_2d": lambda: fq.compress(wide[:, :4096], payload=pays[0]),
+        "compress_2d_blocks": lambda: fq.compress(nar[:, :1024], payload=pays[0]),
+        "roundtrip_2d_blocks": lambda: fq.roundtrip(nar[:, :1024], y=nar_y[:, :1024]),
+    }
+    fn = (lambda: fq.reduce_requantize(pays, n, out=out, scales=sc)) if R else fns[base]
+    ms = timer.median_ms(fn, args.iters)
+    require_no_fault(fq, f"--kernel {k}")
+    peak, _ = measured_peak()
+    print(json.dumps(kernel_record(base, n, ms, peak, 32 if sc == "e8m0" else 16, sc, variant=k)), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ GPU arm
 
-def main():
-    args = parse()
+def main(argv=None):
+    args = parse(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":
         return reference_arm(args, rank, world)
+    if args.kernel:
+        return kernel_mode(args)
 
     import numpy as np
     import torch
@@ -265,25 +622,17 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     fq.build()
+    fq.fault_flags(clear=True)
 
-    xs_np, resid_np = make_inputs()
-    n = xs_np[0].size
-    xs = [inputs.bits_to_torch(x.ravel(), dev) for x in xs_np]
-    resid = inputs.bits_to_torch(resid_np.ravel(), dev)
+    x_bits, r_bits = headline_inputs()
+    n = HEADLINE_N
+    x = inputs.bits_to_torch(x_bits, dev)
+    resid = inputs.bits_to_torch(r_bits, dev)
     dst = resid.clone()
-    pb = fq.payload_bytes(n, GROUP, FWHT)
-    pays = [torch.empty(pb, dtype=torch.uint8, device=dev) for _ in range(R_RANKS)]
-    red = torch.empty(pb, dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def flush_l2():
-        # write a buffer larger than L2, then read another one: the reads evict the dirty
-        # lines, so their write-back is not charged to the next timed kernel
-        flush.zero_()
-        clean.sum()
+    pay = torch.empty(fq.payload_bytes(n, GROUP, FWHT), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    names = ["compress"] * R_RANKS + ["reduce", "decompress_accumulate"]
+    timer = Timer(torch, dev, stream)
+    names = ["compress", "decompress_bf16_b1"]
 
     def step(ev=None):
         # ev: None, [start, end] (step boundaries only) or one event before each kernel plus
@@ -292,30 +641,23 @@ def main():
         each = ev is not None and len(ev) > 2
         if ev is not None:
             ev[0].record(stream)
-        for r in range(R_RANKS):
-            fq.compress(xs[r], payload=pays[r], group=GROUP, fwht=FWHT, stream=stream)
-            if each:
-                ev[1 + r].record(stream)
-        fq.reduce_requantize(pays, n, out=red, group=GROUP, fwht=FWHT, stream=stream)
+        fq.compress(x, payload=pay, group=GROUP, fwht=FWHT, stream=stream)
         if each:
-            ev[1 + R_RANKS].record(stream)
-        fq.decompress_accumulate(red, n, dst, beta=1, group=GROUP, fwht=FWHT, stream=stream)
+            ev[1].record(stream)
+        fq.decompress_accumulate(pay, n, dst, beta=1, group=GROUP, fwht=FWHT, stream=stream)
         if ev is not None:
             ev[-1].record(stream)
 
-    # correctness / error report on fresh buffers (not timed)
+    # one step's result from the residual (kept to check the end-to-end path)
     step()
     torch.cuda.synchronize(dev)
-    ref = sum(inputs.bf16_bits_to_f32(x.ravel()).astype(np.float64) for x in xs_np) + \
-        inputs.bf16_bits_to_f32(resid_np.ravel()).astype(np.float64)
-    first_bits = inputs.torch_to_bits(dst)          # one step's result from the residual
-    got = inputs.bf16_bits_to_f32(first_bits).astype(np.float64)
-    delta = ref - inputs.bf16_bits_to_f32(resid_np.ravel()).astype(np.float64)
-    rel_l2 = float(np.linalg.norm(got - ref) / np.linalg.norm(delta))
+    first = dst.clone()
+    dst.copy_(resid)
 
     for _ in range(args.warmup):
-        flush_l2()
+        timer.flush()
         step()
+
     def new_events(count):
         return [[torch.cuda.Event(enable_timing=True) for _ in range(count)] for _ in range(args.steps)]
     events = new_events(2)
@@ -325,22 +667,25 @@ def main():
         torch.cuda.synchronize(dev)
         t0 = time.time()
         for k in range(args.steps):
-            flush_l2()                        # evict the step's working set from L2 (not timed)
+            timer.flush()                    # evict the step's working set from L2 (not timed)
             step(events[k])
         torch.cuda.synchronize(dev)
         t1 = time.time()
         if pg:
             pg.barrier()
         clocks = clk.stop(t0, t1)
-        # kernel pass: the same K steps again with an event between kernels, for the
-        # per-kernel durations behind "kernels" and "roofline" (not part of "value")
-        kevents = new_events(1 + len(names))
-        torch.cuda.synchronize(dev)
-        for k in range(args.steps):
-            flush_l2()
-            step(kevents[k])
-        torch.cuda.synchronize(dev)
-    per_kernel = {name: [] for name in set(names)}
+    require_no_fault(fq, "the timed steps")
+    # kernel pass: the same K steps again with an event between kernels, for the per-kernel
+    # durations behind "kernels" and "roofline" (not part of "value")
+    kevents = new_events(1 + len(names))
+    torch.cuda.synchronize(dev)
+    for k in range(args.steps):
+        timer.flush()
+        step(kevents[k])
+    torch.cuda.synchronize(dev)
+    require_no_fault(fq, "the per-kernel pass")
+
+    per_kernel = {name: [] for name in names}
     step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
     for ev in kevents:
         for i, name in enumerate(names):
@@ -349,30 +694,34 @@ def main():
     if pg:
         dev_ms = max_over_ranks(dev_ms, pg, dev)
     ms_per_step = dev_ms / args.steps
-    bytes_in = R_RANKS * 2 * n
+    bytes_in = 2 * n
     value = job_gbs(bytes_in, args.steps, world, dev_ms)
 
     peak, peak_src = measured_peak()
     kern = {}
     for name, ts in per_kernel.items():
-        mean_ms = statistics.fmean(ts)
-        ach = ALG_BYTES[name] * n / (mean_ms * 1e-3) / 1e9
-        kern[name] = {"ms": round(mean_ms, 5), "launches_per_step": names.count(name),
-                      "alg_gbs": round(ach, 1), "frac_of_peak": round(ach / peak, 4),
-                      "bf16_in_gbs": round((R_RANKS if name == "reduce" else 1) * 2 * n / (mean_ms * 1e-3) / 1e9, 1)}
-    dom = max(kern, key=lambda k: kern[k]["ms"] * kern[k]["launches_per_step"])
-    traffic = ncu_traffic({"compress": "compress_kernel", "reduce": "reduce_kernel",
-                           "decompress_accumulate": "decompress_kernel"}[dom])
+        rec = kernel_record(name, n, statistics.fmean(ts), peak)
+        rec["launches_per_step"] = names.count(name)
+        kern[name] = rec
+    dom = max(kern, key=lambda k: kern[k]["us"] * kern[k]["launches_per_step"])
+    kname = {"compress": "compress_kernel", "decompress_bf16_b1": "decompress_kernel"}[dom]
+    traffic = ncu_traffic(kname, n)
 
-    # end to end through the public API: pinned host inputs in, result back to the host.
-    # Every step copies its own inputs in and reads its own result back inside the timed
-    # region; the copies of step k + 1 run on a copy stream while step k computes (two sets
-    # of input / result buffers), and the read-back runs on a third stream.
-    hx = [inputs.bits_to_torch(x.ravel()).pin_memory() for x in xs_np]
-    hres = inputs.bits_to_torch(resid_np.ravel()).pin_memory()
+    # relative L2 error of the codec on this tensor (the fused roundtrip = decode(compress))
+    y = torch.empty_like(x)
+    fq.roundtrip(x, y=y, group=GROUP, fwht=FWHT)
+    err = rel_l2(torch, y.float(), x.float())
+    del y
+
+    # end to end through the public API: pinned host tensors in, result back to the host.
+    # Every step copies its own input and residual in and reads its own result back inside
+    # the timed region; the copies of step k + 1 run on a copy stream while step k computes
+    # (two sets of device buffers), and the read-back runs on a third stream.
+    hx = inputs.bits_to_torch(x_bits).pin_memory()
+    hres = inputs.bits_to_torch(r_bits).pin_memory()
     hout = torch.empty_like(hres).pin_memory()
-    e2e_steps = max(3, min(args.steps, 50))
-    sets = [([torch.empty_like(x) for x in xs], torch.empty_like(dst)) for _ in range(2)]
+    e2e_steps = max(3, min(args.steps, 10))
+    sets = [(torch.empty_like(x), torch.empty_like(dst)) for _ in range(2)]
     s_in, s_back = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def e2e(steps):
@@ -383,16 +732,13 @@ def main():
             with torch.cuda.stream(s_in):
                 if k >= 2:                                # the set is free once step k-2 is read back
                     s_in.wait_event(backs[k - 2])
-                for r in range(R_RANKS):
-                    sx[r].copy_(hx[r], non_blocking=True)
+                sx.copy_(hx, non_blocking=True)
                 sd.copy_(hres, non_blocking=True)
                 ins.append(ev())
                 ins[-1].record(s_in)
             stream.wait_event(ins[k])
-            for r in range(R_RANKS):
-                fq.compress(sx[r], payload=pays[r], group=GROUP, fwht=FWHT, stream=stream)
-            fq.reduce_requantize(pays, n, out=red, group=GROUP, fwht=FWHT, stream=stream)
-            fq.decompress_accumulate(red, n, sd, beta=1, group=GROUP, fwht=FWHT, stream=stream)
+            fq.compress(sx, payload=pay, group=GROUP, fwht=FWHT, stream=stream)
+            fq.decompress_accumulate(pay, n, sd, beta=1, group=GROUP, fwht=FWHT, stream=stream)
             dones.append(ev())
             dones[-1].record(stream)
             with torch.cuda.stream(s_back):
@@ -410,28 +756,28 @@ def main():
     s_back.wait_event(last)
     e1.record(s_back)
     torch.cuda.synchronize(dev)
+    require_no_fault(fq, "the end-to-end steps")
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    assert np.array_equal(inputs.torch_to_bits(hout), first_bits), "end-to-end result differs from the device step"
-    h2d = (R_RANKS + 1) * 2 * n
-    d2h = 2 * n
+    assert torch.equal(hout.view(torch.int16), first.cpu().view(torch.int16)), \
+        "end-to-end result differs from the device step"
+    h2d, d2h = 2 * bytes_in, bytes_in
+    del sets, hx, hres, hout, first, dst, resid, pay
+    torch.cuda.empty_cache()
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "ranks": R_RANKS, "shape": [TOKENS, HIDDEN], "group": GROUP,
-                   "block": 256, "fwht": FWHT, "parallelism": f"replicas x{world}",
-                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write + {L2_FLUSH_BYTES >> 20} MiB read, outside the step events)"},
+        "data": "synthetic", "config": bench_config(world), "l2": L2_POLICY,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["alg_gbs"], "peak": peak,
                      "unit": "GB/s", "frac": kern[dom]["frac_of_peak"], "traffic": traffic,
-                     "peak_source": peak_src,
-                     "alg_bytes_per_elem": round(ALG_BYTES[dom], 6), "elems_per_launch": n},
+                     "peak_source": peak_src, "alg_bytes_per_elem": kern[dom]["alg_bytes_per_elem"],
+                     "elems_per_launch": n},
         "kernels": kern,
-        "kernels_timing": "second pass of the K steps with a CUDA event between kernels; the events "
-                          "stop each kernel's launch from overlapping the previous kernel's tail, so "
-                          "these durations add up to more than ms_per_step",
-        "rel_l2_error": round(rel_l2, 6),
+        "kernels_timing": "second pass of the K steps with a CUDA event between kernels (mean per launch); "
+                          "the events stop each kernel's launch from overlapping the previous kernel's tail, "
+                          "so these durations add up to more than ms_per_step",
+        "rel_l2_error": round(err, 6),
         "gpu_launches": len(names) * args.steps,
         "clocks": clocks,
         "e2e": {"value": round(world * bytes_in / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
@@ -439,8 +785,16 @@ def main():
         "wall_ms_timed_region": round((t1 - t0) * 1e3, 2),
         "kernel_source_sha256": kernel_source_sha(),
     }
+    if not args.no_configs and rank == 0:
+        cfg = run_configs(torch, dev, fq, inputs, timer, peak, args.config_iters, headline_x=x_bits)
+        require_no_fault(fq, "the per-config records")
+        line["configs_timing"] = (f"each kernel alone, L2 flushed before every launch, median of "
+                                  f"{args.config_iters} launches; mismatches against the CPU oracle")
+        line["configs"] = cfg
+        line["target_70pct_of_hbm"] = target_summary(cfg)
+        line["parity"] = parity_summary(cfg)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = time_oracle(xs_np, resid_np)
+        line["cpu_baseline"] = time_oracle(x_bits, r_bits)
     if pg:
         pg.barrier()
         pg.destroy_process_group()

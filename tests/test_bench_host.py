@@ -6,6 +6,7 @@ not change the generated code) and must change with any code edit; the lookup mu
 the stamped bytes for a matching hash and nothing otherwise.
 """
 import os
+import re
 import shutil
 
 import bench
@@ -54,10 +55,86 @@ def test_ncu_traffic_needs_a_matching_stamp(tmp_path, monkeypatch):
 
 
 def test_committed_summaries_carry_stamps():
-    """Every per-kernel summary of the bench workload records its kernel and source hash."""
-    names = [n for n in os.listdir(os.path.join(bench.ROOT, "profiles"))
-             if n.endswith("_tp_activation_4096x4096.md")]
-    assert names
-    for n in names:
-        text = open(os.path.join(bench.ROOT, "profiles", n)).read()
-        assert "bench-traffic kernel=" in text and "source_sha256=" in text, n
+    """Every committed summary that feeds `roofline.traffic` records its kernel, source hash
+    and bytes in the stamp format the bench reads."""
+    pdir = os.path.join(bench.ROOT, "profiles")
+    stamped = [n for n in os.listdir(pdir) if n.endswith(".md") and "bench-traffic" in open(os.path.join(pdir, n)).read()]
+    assert stamped
+    for n in stamped:
+        text = open(os.path.join(pdir, n)).read()
+        assert re.search(r"bench-traffic kernel=\w+ source_sha256=[0-9a-f]{16} dram_bytes_per_launch=\d+", text), n
+
+
+def test_both_arms_print_the_same_config(monkeypatch, capsys):
+    """The reference arm's config dict is the GPU arm's (bench_config), so the two lines
+    describe one workload; its sample is bounded."""
+    import json
+
+    import numpy as np
+    small = np.arange(4096, dtype=np.uint16) % 200 + 0x3c00
+    monkeypatch.setattr(bench, "headline_inputs", lambda: (small, small[::-1].copy()))
+    monkeypatch.setattr(bench, "REF_SAMPLE", 2048)
+
+    class A:
+        steps, warmup = 2, 1
+    assert bench.reference_arm(A(), rank=0, world=1) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.bench_config(1)
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert "l2" not in line["config"]
+
+
+def test_bench_refuses_to_report_after_a_fault():
+    """A set fault word (read from a stand-in of the binding) stops the report."""
+    import pytest
+
+    class FakeFq:
+        def __init__(self, word):
+            self.word, self.cleared = word, False
+
+        def fault_flags(self, clear=False):
+            w = self.word
+            if clear:
+                self.word, self.cleared = 0, True
+            return w
+
+    ok = FakeFq(0)
+    bench.require_no_fault(ok, "steps")
+    assert ok.cleared
+    with pytest.raises(bench.FaultWordSet, match="0x1"):
+        bench.require_no_fault(FakeFq(1), "steps")
+    with pytest.raises(bench.FaultWordSet, match="0x6"):
+        bench.require_no_fault(FakeFq(6), "steps")
+
+
+def test_alg_bytes_table():
+    assert bench.alg_bytes("compress") == 2.578125
+    assert bench.alg_bytes("decompress_bf16_b1") == 4.578125
+    assert bench.alg_bytes("roundtrip") == 4.0
+    assert bench.alg_bytes("reduce_r4") == 5 * 0.578125
+    assert bench.alg_bytes("compress", group=32) == 2 + 0.5 + 1 / 32 + 4 / 256
+    assert bench.alg_bytes("compress", scales="e8m0") == 2.53125
+
+
+def test_ncu_traffic_scales_a_smaller_capture(tmp_path, monkeypatch):
+    _tree(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    sha = bench.kernel_source_sha()
+    (prof / "d.md").write_text(
+        f"bench-traffic kernel=decompress_kernel source_sha256={sha} dram_bytes_per_launch=1000 elements=256\n")
+    assert bench.ncu_traffic("decompress_kernel", 1024) == 4000
+    assert bench.ncu_traffic("decompress_kernel") == 1000
+
+
+def test_target_summary_counts_only_large_workloads():
+    cfg = {"small": {"bytes_bf16": 1 << 20, "kernels": [{"kernel": "compress", "frac_of_peak": 0.1}]},
+           "big": {"bytes_bf16": 1 << 27, "kernels": [{"kernel": "compress", "frac_of_peak": 0.75},
+                                                      {"kernel": "roundtrip", "frac_of_peak": 0.65,
+                                                       "group": 32, "fwht": 0}]}}
+    s = bench.target_summary(cfg)
+    assert s["records"] == 2 and s["met"] == 1
+    assert s["below"] == [{"big:roundtrip_g32_fwht0": 0.65}]
