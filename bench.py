@@ -17,7 +17,7 @@ The same JSON line carries one record per workload ("configs"): the toy [8, 512]
 with a 2-rank reduce, the [4096, 4096] TP activation, the emulated 4-rank reduce of
 4 x [8192, 4096] (plus R = 2 and R = 8 on the same payloads), the [16384, 4096] gradient at
 G = 16/32 with the transform on and off, and the size sweep 2^15 ... 2^29. Each kernel there
-is timed alone with cold inputs (L2 flushed before every launch; median of the launches)
+is timed alone with cold inputs (L2 flushed before every launch; mean of the launches)
 and carries its algorithmic GB/s, its fraction of the HBM peak, its code / value mismatches
 against the CPU oracle and the workload's relative L2 error.
 
@@ -96,7 +96,7 @@ def parse(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload records")
-    ap.add_argument("--config-iters", type=int, default=10, help="timed launches per per-config kernel")
+    ap.add_argument("--config-iters", type=int, default=20, help="timed launches per per-config kernel")
     ap.add_argument("--kernel", default=None, help="time one kernel alone and exit: compress, decompress_{bf16,f32}_b{0,1}, roundtrip, reduce_r<R>, "
                     "copy_bf16, compress_f32, roundtrip_f32, compress_2d, compress_2d_blocks, roundtrip_2d_blocks; "
                     "a _mx suffix selects the E8M0 scales")
@@ -331,7 +331,7 @@ class Timer:
         self.flush_buf.zero_()
         self.clean.sum()
 
-    def median_ms(self, fn, iters, warm=3):
+    def mean_ms(self, fn, iters, warm=3):
         torch = self.torch
         ts = []
         for i in range(iters + warm):
@@ -343,7 +343,9 @@ class Timer:
             torch.cuda.synchronize(self.dev)
             if i >= warm:
                 ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+        # the mean, not the median: event timestamps on this part advance in steps of about
+        # 2 us, and the mean of many launches averages that quantisation out
+        return statistics.fmean(ts)
 
 
 def rel_l2(torch, got, ref):
@@ -412,11 +414,11 @@ def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
         y = torch.empty_like(x)
         for k in kernels:
             if k == "compress":
-                ms = timer.median_ms(lambda: fq.compress(x, payload=pay, **kw), iters)
+                ms = timer.mean_ms(lambda: fq.compress(x, payload=pay, **kw), iters)
                 recs.append(kernel_record(k, n, ms, peak, group, code_mismatches=cmis, scale_byte_mismatches=smis))
             elif k.startswith("decompress"):
                 beta = int(k[-1])
-                ms = timer.median_ms(lambda: fq.decompress_accumulate(pay, n, dst, beta=beta, **kw), iters)
+                ms = timer.mean_ms(lambda: fq.decompress_accumulate(pay, n, dst, beta=beta, **kw), iters)
                 dst.copy_(dst0)
                 fq.decompress_accumulate(pay, n, dst, beta=beta, **kw)
                 d0 = inputs.torch_to_bits(dst0)
@@ -424,7 +426,7 @@ def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
                 vm = int(np.count_nonzero(inputs.torch_to_bits(dst) != ref))
                 recs.append(kernel_record(k, n, ms, peak, group, value_mismatches=vm))
             elif k == "roundtrip":
-                ms = timer.median_ms(lambda: fq.roundtrip(x, y=y, **kw), iters)
+                ms = timer.mean_ms(lambda: fq.roundtrip(x, y=y, **kw), iters)
                 # roundtrip = decode(compress(x)) with beta = 0: against the oracle's decode of
                 # its own payload
                 ref = oracle.decompress_accumulate(want, n, np.zeros(n, np.uint16), beta=0, group=group, fwht=fwht)
@@ -441,7 +443,7 @@ def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
     recs, err = codec_records(xs[0], "toy", kernels=("compress", "decompress_bf16_b1", "roundtrip"))
     pays = [fq.compress(to_dev(x)) for x in xs]
     red = fq.reduce_requantize(pays, n)
-    ms = timer.median_ms(lambda: fq.reduce_requantize(pays, n, out=red), iters)
+    ms = timer.mean_ms(lambda: fq.reduce_requantize(pays, n, out=red), iters)
     want = oracle.reduce_requantize([oracle.compress(x) for x in xs], n)
     cm, sm = payload_mismatch(red.cpu().numpy(), want, n)
     dec = torch.empty(n, dtype=torch.bfloat16, device=dev)
@@ -465,7 +467,7 @@ def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
     pays = [fq.compress(x) for x in xt]
     wants = [oracle.compress(x) for x in xs]
     cm = [payload_mismatch(p.cpu().numpy(), w, n) for p, w in zip(pays, wants)]
-    recs = [kernel_record("compress", n, timer.median_ms(lambda: fq.compress(xt[0], payload=pays[0]), iters), peak,
+    recs = [kernel_record("compress", n, timer.mean_ms(lambda: fq.compress(xt[0], payload=pays[0]), iters), peak,
                           code_mismatches=sum(c for c, _ in cm), scale_byte_mismatches=sum(s for _, s in cm),
                           note="rank 0 timed; parity over all 4 ranks")]
     red = torch.empty_like(pays[0])
@@ -474,13 +476,13 @@ def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
     for R in (4, 2, 8):
         sel = [i % 4 for i in range(R)]
         ps = [pays[i] for i in sel]
-        ms = timer.median_ms(lambda: fq.reduce_requantize(ps, n, out=red), iters)
+        ms = timer.mean_ms(lambda: fq.reduce_requantize(ps, n, out=red), iters)
         fq.reduce_requantize(ps, n, out=red)
         want = oracle.reduce_requantize([wants[i] for i in sel], n)
         c, s_ = payload_mismatch(red.cpu().numpy(), want, n)
         recs.append(kernel_record(f"reduce_r{R}", n, ms, peak, code_mismatches=c, scale_byte_mismatches=s_))
         if R == 4:
-            ms = timer.median_ms(lambda: fq.decompress_accumulate(red, n, dec, beta=0), iters)
+            ms = timer.mean_ms(lambda: fq.decompress_accumulate(red, n, dec, beta=0), iters)
             fq.decompress_accumulate(red, n, dec, beta=0)
             ref = oracle.decompress_accumulate(red.cpu().numpy(), n, np.zeros(n, np.uint16), beta=0)
             recs.append(kernel_record("decompress_bf16_b0", n, ms, peak,
@@ -589,7 +591,7 @@ def kernel_mode(args):
         "roundtrip_2d_blocks": lambda: fq.roundtrip(nar[:, :1024], y=nar_y[:, :1024]),
     }
     fn = (lambda: fq.reduce_requantize(pays, n, out=out, scales=sc)) if R else fns[base]
-    ms = timer.median_ms(fn, args.iters)
+    ms = timer.mean_ms(fn, args.iters)
     require_no_fault(fq, f"--kernel {k}")
     peak, _ = measured_peak()
     print(json.dumps(kernel_record(base, n, ms, peak, 32 if sc == "e8m0" else 16, sc, variant=k)), flush=True)
@@ -788,7 +790,7 @@ def main(argv=None):
     if not args.no_configs and rank == 0:
         cfg = run_configs(torch, dev, fq, inputs, timer, peak, args.config_iters, headline_x=x_bits)
         require_no_fault(fq, "the per-config records")
-        line["configs_timing"] = (f"each kernel alone, L2 flushed before every launch, median of "
+        line["configs_timing"] = (f"each kernel alone, L2 flushed before every launch, mean of "
                                   f"{args.config_iters} launches; mismatches against the CPU oracle")
         line["configs"] = cfg
         line["target_70pct_of_hbm"] = target_summary(cfg)

@@ -37,8 +37,9 @@ from . import _lib
 from ._lib import BF16, F32, Fp4qError, build  # noqa: F401
 
 __all__ = ["payload_bytes", "gscale_offset", "bscale_offset", "compress",
-           "decompress_accumulate", "roundtrip", "reduce_requantize", "build", "Fp4qError",
-           "Fp4qFault", "library_path", "fault_flags"]
+           "decompress_accumulate", "roundtrip", "reduce_requantize", "segment_bytes",
+           "compress_segments", "decompress_accumulate_segments", "reduce_requantize_segments",
+           "build", "Fp4qError", "Fp4qFault", "library_path", "fault_flags"]
 
 
 class Fp4qFault(RuntimeError):
@@ -241,6 +242,87 @@ def reduce_requantize(payloads, n: int, out=None, group: int | None = None, fwht
     st = _lib.lib().fp4q_reduce_requantize(ctypes.cast(ptrs, ctypes.c_void_p), R, int(n), po, ctypes.byref(p),
                                            _stream(stream, device))
     _lib.check("fp4q_reduce_requantize", st)
+    _fault_check(device, check)
+    return out
+
+
+# ------------------------------------------------------------------ payloads as separate segments
+
+def segment_bytes(n: int, group: int | None = None, fwht: int = 1, scales: str = "dual"):
+    """(codes, group scales, block scales) bytes of a payload of n elements placed as three
+    separate segments (block scales 0 for E8M0 scales)."""
+    p = _lib.params(group, fwht, scales=scales)
+    c, g, b = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _lib.check("fp4q_segment_bytes", _lib.lib().fp4q_segment_bytes(int(n), ctypes.byref(p), ctypes.byref(c),
+                                                                    ctypes.byref(g), ctypes.byref(b)))
+    return int(c.value), int(g.value), int(b.value)
+
+
+def _segments(segs, n, group, fwht, scales, device, name):
+    """fp4q_segments of a (codes, gscales, bscales) tuple of uint8 CUDA tensors, each checked
+    to be large enough (bscales may be None for E8M0 scales)."""
+    if len(segs) != 3:
+        raise ValueError(f"{name} must be (codes, gscales, bscales)")
+    sizes = segment_bytes(n, group, fwht, scales)
+    ptrs = []
+    for t, need, part in zip(segs, sizes, ("codes", "gscales", "bscales")):
+        if need == 0 and t is None:
+            ptrs.append(None)
+            continue
+        ptrs.append(_buffer(t, f"{name}.{part}", need, device).value)
+    return _lib.Segments(*ptrs)
+
+
+def compress_segments(x, segs, group: int | None = None, fwht: int = 1, stream=None, scales: str = "dual",
+                      check: bool = False):
+    """compress(x) writing the payload into three separate uint8 buffers (codes, gscales,
+    bscales); bit-identical to the contiguous payload's segments."""
+    import torch
+    _cuda_data(x, "x")
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("x must be bfloat16 or float32")
+    sg = _segments(segs, x.numel(), group, fwht, scales, x.device, "segs")
+    p = _lib.params(group, fwht, scales=scales)
+    st = _lib.lib().fp4q_compress_segments(_dev(x, "x"), BF16 if x.dtype == torch.bfloat16 else F32, x.numel(),
+                                           ctypes.byref(sg), ctypes.byref(p), _stream(stream, x.device))
+    _lib.check("fp4q_compress_segments", st)
+    _fault_check(x.device, check)
+    return segs
+
+
+def decompress_accumulate_segments(segs, n: int, dst, beta: int = 1, group: int | None = None, fwht: int = 1,
+                                   stream=None, scales: str = "dual", check: bool = False):
+    """decompress_accumulate reading the payload from three separate segments."""
+    import torch
+    _cuda_data(dst, "dst")
+    if dst.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("dst must be bfloat16 or float32")
+    if dst.numel() != n:
+        raise ValueError("dst must have n elements")
+    sg = _segments(segs, n, group, fwht, scales, dst.device, "segs")
+    p = _lib.params(group, fwht, scales=scales)
+    st = _lib.lib().fp4q_decompress_accumulate_segments(ctypes.byref(sg), int(n), _dev(dst, "dst"),
+                                                        BF16 if dst.dtype == torch.bfloat16 else F32, int(beta),
+                                                        ctypes.byref(p), _stream(stream, dst.device))
+    _lib.check("fp4q_decompress_accumulate_segments", st)
+    _fault_check(dst.device, check)
+    return dst
+
+
+def reduce_requantize_segments(ins, n: int, out, group: int | None = None, fwht: int = 1, stream=None,
+                               scales: str = "dual", check: bool = False):
+    """reduce_requantize over R payloads given as segment tuples, into the segments of out."""
+    R = len(ins)
+    if R < 1:
+        raise ValueError("reduce_requantize_segments needs at least one input")
+    _cuda_data(out[0], "out.codes")
+    device = out[0].device
+    arr = (_lib.Segments * R)(*[_segments(sg, n, group, fwht, scales, device, f"ins[{i}]") for i, sg in enumerate(ins)])
+    so = _segments(out, n, group, fwht, scales, device, "out")
+    p = _lib.params(group, fwht, scales=scales)
+    st = _lib.lib().fp4q_reduce_requantize_segments(arr, R, int(n), ctypes.byref(so), ctypes.byref(p),
+                                                    _stream(stream, device))
+    _lib.check("fp4q_reduce_requantize_segments", st)
     _fault_check(device, check)
     return out
 

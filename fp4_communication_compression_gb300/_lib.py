@@ -30,7 +30,9 @@ BF16, F32 = 0, 1
 EXPORTS = ["fp4q_payload_bytes", "fp4q_gscale_offset", "fp4q_bscale_offset", "fp4q_compress",
            "fp4q_compress_f32", "fp4q_decompress_accumulate", "fp4q_roundtrip", "fp4q_roundtrip_f32",
            "fp4q_compress_2d", "fp4q_decompress_accumulate_2d", "fp4q_roundtrip_2d",
-           "fp4q_reduce_requantize", "fp4q_fault_flags", "fp4q_selftest_wait_timeout",
+           "fp4q_reduce_requantize", "fp4q_segment_bytes", "fp4q_compress_segments",
+           "fp4q_decompress_accumulate_segments", "fp4q_reduce_requantize_segments",
+           "fp4q_fault_flags", "fp4q_selftest_wait_timeout",
            "fp4q_status_string", "fp4q_version"]
 
 
@@ -46,6 +48,11 @@ SCALES = {"dual": 0, "e8m0": 1}   # fp4q_params.scales: FP4Q_SCALES_DUAL, FP4Q_S
 class Params(ctypes.Structure):
     _fields_ = [("group", ctypes.c_int32), ("block", ctypes.c_int32), ("fwht", ctypes.c_int32),
                 ("scales", ctypes.c_int32)]
+
+
+class Segments(ctypes.Structure):
+    """fp4q_segments: device pointers of a payload's codes, group scales and block scales."""
+    _fields_ = [("codes", ctypes.c_void_p), ("gscales", ctypes.c_void_p), ("bscales", ctypes.c_void_p)]
 
 
 def build(force: bool = False, nvcc: str = "nvcc") -> str:
@@ -80,6 +87,8 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
         pp = ctypes.POINTER(Params)
+        ps = ctypes.POINTER(Segments)
+        SZP = ctypes.POINTER(ctypes.c_size_t)
         sig = {
             "fp4q_payload_bytes": (SZ, [I64, pp]),
             "fp4q_gscale_offset": (SZ, [I64, pp]),
@@ -93,6 +102,10 @@ def lib():
             "fp4q_decompress_accumulate": (ctypes.c_int, [P, I64, P, ctypes.c_int, I32, pp, P]),
             "fp4q_roundtrip": (ctypes.c_int, [P, I64, P, pp, P]),
             "fp4q_reduce_requantize": (ctypes.c_int, [P, I32, I64, P, pp, P]),
+            "fp4q_segment_bytes": (ctypes.c_int, [I64, pp, SZP, SZP, SZP]),
+            "fp4q_compress_segments": (ctypes.c_int, [P, ctypes.c_int, I64, ps, pp, P]),
+            "fp4q_decompress_accumulate_segments": (ctypes.c_int, [ps, I64, P, ctypes.c_int, I32, pp, P]),
+            "fp4q_reduce_requantize_segments": (ctypes.c_int, [ps, I32, I64, ps, pp, P]),
             "fp4q_fault_flags": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), I32]),
             "fp4q_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, P]),
             "fp4q_status_string": (ctypes.c_char_p, [ctypes.c_int]),

@@ -1813,9 +1813,8 @@ fp4q_status launch_tail(K kernel, cudaStream_t s, Args&&... args) {
 // Full blocks through the tiled kernel, then the zero-padded last block (if any) through
 // the one-warp tail kernel; the payload layout is that of the padded length.
 template <int G, int F, bool MX, bool XF>
-fp4q_status launch_compress(const void* x, int64_t n, void* payload, cudaStream_t s) {
+fp4q_status launch_compress(const void* x, int64_t n, const Payload& P, cudaStream_t s) {
   const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
-  const Payload P = payload_of(payload, padded_n(n), G, MX);
   if (nfull > 0) {
     TileLoop T = tiles_of(nfull);
     CUtensorMap xm;
@@ -1834,9 +1833,8 @@ fp4q_status launch_compress(const void* x, int64_t n, void* payload, cudaStream_
 }
 
 template <int G, int F, int DT, int B, bool MX>
-fp4q_status launch_decompress(const void* payload, int64_t n, void* dst, cudaStream_t s) {
+fp4q_status launch_decompress(const Payload& P, int64_t n, void* dst, cudaStream_t s) {
   const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
-  const Payload P = payload_of(const_cast<void*>(payload), padded_n(n), G, MX);
   if (nfull > 0) {
     TileLoop T = tiles_of(nfull);
     CUtensorMap dm;
@@ -1932,10 +1930,9 @@ fp4q_status launch_roundtrip_2d(const void* x, int64_t rows, int64_t cols, int64
 }
 
 template <int G, int R, bool MX>
-fp4q_status launch_reduce_r(const RankPtrs& in, int64_t n, void* out, cudaStream_t s) {
+fp4q_status launch_reduce_r(const RankPtrs& in, int64_t n, const Payload& P, cudaStream_t s) {
   n = padded_n(n);   // the reduce works on whole (zero-padded) blocks of the payloads
   TileLoop T = tiles_of(n);
-  const Payload P = payload_of(out, n, G, MX);
   const int sms = num_sms();
   const bool dyn = sms > 0 && T.tiles >= kReduceDynTilesPerSm * sms;
   auto k = dyn ? reduce_kernel<G, R, MX, true> : reduce_kernel<G, R, MX, false>;
@@ -1947,14 +1944,13 @@ fp4q_status launch_reduce_r(const RankPtrs& in, int64_t n, void* out, cudaStream
 }
 
 template <int G, bool MX>
-fp4q_status launch_reduce(const void* const* payloads, int R, int64_t n, void* out, cudaStream_t s) {
+fp4q_status launch_reduce(const Payload* ins, int R, int64_t n, const Payload& out, cudaStream_t s) {
   RankPtrs in;
   memset(&in, 0, sizeof(in));
   for (int r = 0; r < R; ++r) {
-    const Payload p = payload_of(const_cast<void*>(payloads[r]), padded_n(n), G, MX);
-    in.codes[r] = p.codes;
-    in.gsc[r] = p.gsc;
-    in.bsc[r] = p.bsc;
+    in.codes[r] = ins[r].codes;
+    in.gsc[r] = ins[r].gsc;
+    in.bsc[r] = ins[r].bsc;
   }
   switch (R) {
     case 1: return launch_reduce_r<G, 1, MX>(in, n, out, s);
@@ -1974,7 +1970,7 @@ size_t payload_bytes_of(int64_t n, int G, bool mx) {
 }
 
 template <int G, bool MX>
-fp4q_status dispatch_decompress(int key, const void* payload, int64_t n, void* dst, cudaStream_t s) {
+fp4q_status dispatch_decompress(int key, const Payload& payload, int64_t n, void* dst, cudaStream_t s) {
   switch (key) {
     case 0: return launch_decompress<G, 0, FP4Q_BF16, 0, MX>(payload, n, dst, s);
     case 1: return launch_decompress<G, 0, FP4Q_BF16, 1, MX>(payload, n, dst, s);
@@ -1985,6 +1981,26 @@ fp4q_status dispatch_decompress(int key, const void* payload, int64_t n, void* d
     case 6: return launch_decompress<G, 1, FP4Q_F32, 0, MX>(payload, n, dst, s);
     default: return launch_decompress<G, 1, FP4Q_F32, 1, MX>(payload, n, dst, s);
   }
+}
+
+template <bool XF>
+fp4q_status dispatch_compress(int G, int F, bool MX, const void* x, int64_t n, const Payload& P, cudaStream_t s) {
+  if (MX) return F ? launch_compress<32, 1, true, XF>(x, n, P, s) : launch_compress<32, 0, true, XF>(x, n, P, s);
+  if (G == 16) return F ? launch_compress<16, 1, false, XF>(x, n, P, s) : launch_compress<16, 0, false, XF>(x, n, P, s);
+  return F ? launch_compress<32, 1, false, XF>(x, n, P, s) : launch_compress<32, 0, false, XF>(x, n, P, s);
+}
+
+template <bool MX>
+fp4q_status dispatch_reduce(int G, const Payload* ins, int R, int64_t n, const Payload& out, cudaStream_t s) {
+  if (MX) return launch_reduce<32, true>(ins, R, n, out, s);
+  return G == 16 ? launch_reduce<16, false>(ins, R, n, out, s) : launch_reduce<32, false>(ins, R, n, out, s);
+}
+
+fp4q_status dispatch_decompress_all(int G, int F, bool MX, const Payload& P, int64_t n, void* dst, fp4q_dtype dtype,
+                                    int beta, cudaStream_t s) {
+  const int key = F * 4 + (dtype == FP4Q_F32) * 2 + beta;
+  if (MX) return dispatch_decompress<32, true>(key, P, n, dst, s);
+  return G == 16 ? dispatch_decompress<16, false>(key, P, n, dst, s) : dispatch_decompress<32, false>(key, P, n, dst, s);
 }
 
 // Argument checks and dispatch of compress / roundtrip for BF16 (XF = false) or FP32 input.
@@ -1998,10 +2014,7 @@ fp4q_status compress_entry(const void* x, int64_t n, void* payload, const fp4q_p
   if (!size_ok(n)) return FP4Q_ERR_SIZE;
   if (!aligned16(x) || !aligned16(payload)) return FP4Q_ERR_ALIGN;
   if (overlap(x, (size_t)n * (XF ? 4 : 2), payload, payload_bytes_of(n, G, MX))) return FP4Q_ERR_OVERLAP;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (MX) return F ? launch_compress<32, 1, true, XF>(x, n, payload, s) : launch_compress<32, 0, true, XF>(x, n, payload, s);
-  if (G == 16) return F ? launch_compress<16, 1, false, XF>(x, n, payload, s) : launch_compress<16, 0, false, XF>(x, n, payload, s);
-  return F ? launch_compress<32, 1, false, XF>(x, n, payload, s) : launch_compress<32, 0, false, XF>(x, n, payload, s);
+  return dispatch_compress<XF>(G, F, MX, x, n, payload_of(payload, padded_n(n), G, MX), static_cast<cudaStream_t>(stream));
 }
 
 template <bool XF>
@@ -2019,6 +2032,40 @@ fp4q_status roundtrip_entry(const void* x, int64_t n, void* y, const fp4q_params
   if (MX) return F ? launch_roundtrip<32, 1, true, XF>(x, n, y, s) : launch_roundtrip<32, 0, true, XF>(x, n, y, s);
   if (G == 16) return F ? launch_roundtrip<16, 1, false, XF>(x, n, y, s) : launch_roundtrip<16, 0, false, XF>(x, n, y, s);
   return F ? launch_roundtrip<32, 1, false, XF>(x, n, y, s) : launch_roundtrip<32, 0, false, XF>(x, n, y, s);
+}
+
+// A payload given as three separately placed segments (fp4q_segments): each 16-byte aligned,
+// sized as in the contiguous payload of n elements (codes m/2, group scales pad16(m/G), block
+// scales 4 m/256 bytes, m = n rounded up to whole blocks); the block scales are absent (NULL)
+// for E8M0 scales.
+struct SegSizes {
+  size_t codes, gsc, bsc;
+};
+SegSizes seg_sizes(int64_t n, int G, bool mx) {
+  const int64_t m = padded_n(n);
+  return {(size_t)(m / 2), (size_t)pad16(m / G), mx ? (size_t)0 : (size_t)(4 * (m / FP4Q_BLOCK))};
+}
+fp4q_status segments_of(const fp4q_segments* sg, int64_t n, int G, bool mx, Payload& P) {
+  if (!sg || !sg->codes || !sg->gscales || (!mx && !sg->bscales)) return FP4Q_ERR_NULL;
+  if (!aligned16(sg->codes) || !aligned16(sg->gscales) || (!mx && !aligned16(sg->bscales))) return FP4Q_ERR_ALIGN;
+  P.codes = static_cast<uint8_t*>(sg->codes);
+  P.gsc = static_cast<uint8_t*>(sg->gscales);
+  P.bsc = mx ? nullptr : static_cast<float*>(sg->bscales);
+  P.nb = padded_n(n) / FP4Q_BLOCK;
+  return FP4Q_OK;
+}
+// Does any segment of P overlap [a, a + na)?
+bool seg_overlap(const Payload& P, const SegSizes& z, const void* a, size_t na) {
+  return overlap(P.codes, z.codes, a, na) || overlap(P.gsc, z.gsc, a, na) || (P.bsc && overlap(P.bsc, z.bsc, a, na));
+}
+// Do two segment sets overlap anywhere (or, with self, do a set's own segments overlap)?
+bool segs_overlap(const Payload& A, const Payload& B, const SegSizes& z) {
+  return seg_overlap(B, z, A.codes, z.codes) || seg_overlap(B, z, A.gsc, z.gsc) ||
+         (A.bsc && seg_overlap(B, z, A.bsc, z.bsc));
+}
+bool segs_self_overlap(const Payload& P, const SegSizes& z) {
+  return overlap(P.codes, z.codes, P.gsc, z.gsc) ||
+         (P.bsc && (overlap(P.codes, z.codes, P.bsc, z.bsc) || overlap(P.gsc, z.gsc, P.bsc, z.bsc)));
 }
 
 // A strided 2-D view: rows >= 1, cols a positive multiple of 256, rows * cols < 2^37,
@@ -2081,11 +2128,8 @@ fp4q_status fp4q_decompress_accumulate(const void* payload, int64_t n, void* dst
   if (!aligned16(payload) || !aligned16(dst)) return FP4Q_ERR_ALIGN;
   const size_t dbytes = (size_t)n * (dtype == FP4Q_BF16 ? 2 : 4);
   if (overlap(payload, payload_bytes_of(n, G, MX), dst, dbytes)) return FP4Q_ERR_OVERLAP;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int key = F * 4 + (dtype == FP4Q_F32) * 2 + beta;
-  if (MX) return dispatch_decompress<32, true>(key, payload, n, dst, s);
-  return G == 16 ? dispatch_decompress<16, false>(key, payload, n, dst, s)
-                 : dispatch_decompress<32, false>(key, payload, n, dst, s);
+  return dispatch_decompress_all(G, F, MX, payload_of(const_cast<void*>(payload), padded_n(n), G, MX), n, dst, dtype,
+                                 beta, static_cast<cudaStream_t>(stream));
 }
 
 fp4q_status fp4q_roundtrip(const void* x_bf16, int64_t n, void* y_bf16, const fp4q_params* params,
@@ -2190,10 +2234,82 @@ fp4q_status fp4q_reduce_requantize(const void* const* payloads, int32_t R, int64
   const size_t pb = payload_bytes_of(n, G, MX);
   for (int r = 0; r < R; ++r)
     if (overlap(payloads[r], pb, out_payload, pb)) return FP4Q_ERR_OVERLAP;
+  Payload ins[FP4Q_MAX_RANKS];
+  for (int r = 0; r < R; ++r) ins[r] = payload_of(const_cast<void*>(payloads[r]), padded_n(n), G, MX);
+  const Payload out = payload_of(out_payload, padded_n(n), G, MX);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (MX) return launch_reduce<32, true>(payloads, R, n, out_payload, s);
-  return G == 16 ? launch_reduce<16, false>(payloads, R, n, out_payload, s)
-                 : launch_reduce<32, false>(payloads, R, n, out_payload, s);
+  return MX ? dispatch_reduce<true>(G, ins, R, n, out, s) : dispatch_reduce<false>(G, ins, R, n, out, s);
+}
+
+fp4q_status fp4q_segment_bytes(int64_t n, const fp4q_params* params, size_t* codes, size_t* gscales,
+                               size_t* bscales) {
+  int G, F;
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
+  if (st != FP4Q_OK) return st;
+  if (!codes || !gscales || !bscales) return FP4Q_ERR_NULL;
+  if (!size_ok(n)) return FP4Q_ERR_SIZE;
+  const SegSizes z = seg_sizes(n, G, MX);
+  *codes = z.codes;
+  *gscales = z.gsc;
+  *bscales = z.bsc;
+  return FP4Q_OK;
+}
+
+fp4q_status fp4q_compress_segments(const void* x, fp4q_dtype x_dtype, int64_t n, const fp4q_segments* out,
+                                   const fp4q_params* params, void* stream) {
+  int G, F;
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
+  if (st != FP4Q_OK) return st;
+  if (x_dtype != FP4Q_BF16 && x_dtype != FP4Q_F32) return FP4Q_ERR_PARAM;
+  if (!x || !out) return FP4Q_ERR_NULL;
+  if (!size_ok(n)) return FP4Q_ERR_SIZE;
+  Payload P;
+  if ((st = segments_of(out, n, G, MX, P)) != FP4Q_OK) return st;
+  if (!aligned16(x)) return FP4Q_ERR_ALIGN;
+  const SegSizes z = seg_sizes(n, G, MX);
+  const bool xf = x_dtype == FP4Q_F32;
+  if (segs_self_overlap(P, z) || seg_overlap(P, z, x, (size_t)n * (xf ? 4 : 2))) return FP4Q_ERR_OVERLAP;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return xf ? dispatch_compress<true>(G, F, MX, x, n, P, s) : dispatch_compress<false>(G, F, MX, x, n, P, s);
+}
+
+fp4q_status fp4q_decompress_accumulate_segments(const fp4q_segments* in, int64_t n, void* dst, fp4q_dtype dtype,
+                                                int32_t beta, const fp4q_params* params, void* stream) {
+  int G, F;
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
+  if (st != FP4Q_OK) return st;
+  if ((dtype != FP4Q_BF16 && dtype != FP4Q_F32) || (beta != 0 && beta != 1)) return FP4Q_ERR_PARAM;
+  if (!in || !dst) return FP4Q_ERR_NULL;
+  if (!size_ok(n)) return FP4Q_ERR_SIZE;
+  Payload P;
+  if ((st = segments_of(in, n, G, MX, P)) != FP4Q_OK) return st;
+  if (!aligned16(dst)) return FP4Q_ERR_ALIGN;
+  if (seg_overlap(P, seg_sizes(n, G, MX), dst, (size_t)n * (dtype == FP4Q_BF16 ? 2 : 4))) return FP4Q_ERR_OVERLAP;
+  return dispatch_decompress_all(G, F, MX, P, n, dst, dtype, beta, static_cast<cudaStream_t>(stream));
+}
+
+fp4q_status fp4q_reduce_requantize_segments(const fp4q_segments* in, int32_t R, int64_t n, const fp4q_segments* out,
+                                            const fp4q_params* params, void* stream) {
+  int G, F;
+  bool MX;
+  fp4q_status st = check_params(params, G, F, MX);
+  if (st != FP4Q_OK) return st;
+  if (R < 1 || R > FP4Q_MAX_RANKS) return FP4Q_ERR_PARAM;
+  if (!in || !out) return FP4Q_ERR_NULL;
+  if (!size_ok(n)) return FP4Q_ERR_SIZE;
+  Payload ins[FP4Q_MAX_RANKS], P;
+  for (int r = 0; r < R; ++r)
+    if ((st = segments_of(&in[r], n, G, MX, ins[r])) != FP4Q_OK) return st;
+  if ((st = segments_of(out, n, G, MX, P)) != FP4Q_OK) return st;
+  const SegSizes z = seg_sizes(n, G, MX);
+  if (segs_self_overlap(P, z)) return FP4Q_ERR_OVERLAP;
+  for (int r = 0; r < R; ++r)
+    if (segs_overlap(ins[r], P, z)) return FP4Q_ERR_OVERLAP;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return MX ? dispatch_reduce<true>(G, ins, R, n, P, s) : dispatch_reduce<false>(G, ins, R, n, P, s);
 }
 
 fp4q_status fp4q_fault_flags(uint32_t* flags, int32_t clear) {

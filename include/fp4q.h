@@ -208,6 +208,42 @@ fp4q_status fp4q_reduce_requantize(const void* const* payloads, int32_t R, int64
                                    void* out_payload, const fp4q_params* params,
                                    void* stream);
 
+/* A payload placed as three separate device buffers instead of one contiguous one (the
+ * Payload step above, segment by segment): codes (m/2 bytes), group scales (m/G bytes
+ * zero-padded to a multiple of 16) and block scales (4 m/256 bytes; NULL for E8M0 scales),
+ * m = n rounded up to a multiple of 256. Each pointer must be 16-byte aligned. The segments
+ * of a tensor's payload can then be cut at block boundaries and scattered / gathered by a
+ * collective (reduce-scatter, all-gather) without any repacking: the compressed AllReduce
+ * of tensor parallelism [P3 "Read it as"] exchanges exactly such slices. */
+typedef struct fp4q_segments {
+  void* codes;
+  void* gscales;
+  void* bscales;
+} fp4q_segments;
+
+/* Sizes in bytes of the three segments of a payload of n elements (as above); bscales is 0
+ * for E8M0 scales. Errors: FP4Q_ERR_PARAM, FP4Q_ERR_NULL, FP4Q_ERR_SIZE. */
+fp4q_status fp4q_segment_bytes(int64_t n, const fp4q_params* params, size_t* codes, size_t* gscales,
+                               size_t* bscales);
+
+/* fp4q_compress / fp4q_compress_f32 (x_dtype FP4Q_BF16 or FP4Q_F32) writing the payload into
+ * separately placed segments. Bit-identical to the contiguous call. No segment may overlap x
+ * or another segment (FP4Q_ERR_OVERLAP). */
+fp4q_status fp4q_compress_segments(const void* x, fp4q_dtype x_dtype, int64_t n, const fp4q_segments* out,
+                                   const fp4q_params* params, void* stream);
+
+/* fp4q_decompress_accumulate reading a payload from separately placed segments. */
+fp4q_status fp4q_decompress_accumulate_segments(const fp4q_segments* in, int64_t n, void* dst, fp4q_dtype dtype,
+                                                int32_t beta, const fp4q_params* params, void* stream);
+
+/* fp4q_reduce_requantize over R payloads given as segments (in: a HOST array of R segment
+ * sets), writing the requantized sum into the segments of out. This is the shard owner's
+ * step of a compressed reduce-scatter: in[r] are the slices of rank r's payload that cover
+ * the owner's shard, in rank order [P3 "Read it as": the AllReduce of tensor parallelism].
+ * 1 <= R <= FP4Q_MAX_RANKS; out may not overlap any input or itself. */
+fp4q_status fp4q_reduce_requantize_segments(const fp4q_segments* in, int32_t R, int64_t n, const fp4q_segments* out,
+                                            const fp4q_params* params, void* stream);
+
 /* Device fault word of the current device. The kernels wait on TMA copies with bounded
  * waits (about a second); a wait that gives up sets a bit here, waits (bounded) for the
  * warp's copies still in flight and returns early, leaving that call's outputs incomplete:

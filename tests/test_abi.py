@@ -196,3 +196,59 @@ def test_2d_entry_points_argument_errors(L):
     assert d2(A, 4, 512, B, 1024, 7, 1, pp, None) == _lib.ERR_PARAM
     assert r2(A, 4, 512, 1024, B, 256, pp, None) == _lib.ERR_PARAM
     assert r2(A, 4, 512, 1024, A + 1024, 1024, pp, None) == _lib.ERR_OVERLAP
+
+
+def _seg(c, g, b):
+    return _lib.Segments(c, g, b)
+
+
+def test_segment_bytes(L):
+    c, g, b = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    for n, G, sc in [(4096, 16, "dual"), (256 * 37 + 5, 32, "dual"), (256 * 7, 32, "e8m0"), (1, 16, "dual")]:
+        p = _lib.params(G, 1, scales=sc)
+        assert L.fp4q_segment_bytes(n, ctypes.byref(p), ctypes.byref(c), ctypes.byref(g), ctypes.byref(b)) == _lib.OK
+        total = oracle.payload_bytes(n, G, scales=sc)
+        assert c.value == oracle.gscale_offset(n, G, scales=sc)
+        assert g.value == oracle.bscale_offset(n, G, scales=sc) - c.value
+        assert c.value + g.value + b.value == total
+        assert (b.value == 0) == (sc == "e8m0")
+    assert L.fp4q_segment_bytes(0, ctypes.byref(P), ctypes.byref(c), ctypes.byref(g), ctypes.byref(b)) == _lib.ERR_SIZE
+    assert L.fp4q_segment_bytes(4096, ctypes.byref(P), None, ctypes.byref(g), ctypes.byref(b)) == _lib.ERR_NULL
+    assert L.fp4q_segment_bytes(4096, ctypes.byref(_lib.Params(8, 256, 1)), ctypes.byref(c), ctypes.byref(g),
+                                ctypes.byref(b)) == _lib.ERR_PARAM
+
+
+def test_segment_entry_points_argument_errors(L):
+    pp = ctypes.byref(P)
+    good = _seg(B, B + 0x10000, B + 0x20000)
+    cs, ds, rs = L.fp4q_compress_segments, L.fp4q_decompress_accumulate_segments, L.fp4q_reduce_requantize_segments
+    assert cs(A, _lib.BF16, 4096, None, pp, None) == _lib.ERR_NULL
+    assert cs(None, _lib.BF16, 4096, ctypes.byref(good), pp, None) == _lib.ERR_NULL
+    assert cs(A, _lib.BF16, 4096, ctypes.byref(_seg(B, None, B + 0x20000)), pp, None) == _lib.ERR_NULL
+    assert cs(A, _lib.BF16, 4096, ctypes.byref(_seg(B, B + 0x10000, None)), pp, None) == _lib.ERR_NULL
+    # E8M0 scales have no block-scale segment: NULL passes the null check there (the call is
+    # stopped by the misaligned input instead, before any launch)
+    mx = ctypes.byref(_lib.params(32, 1, scales="e8m0"))
+    assert cs(A + 8, _lib.BF16, 4096, ctypes.byref(_seg(B, B + 0x10000, None)), mx, None) == _lib.ERR_ALIGN
+    assert cs(A, 5, 4096, ctypes.byref(good), pp, None) == _lib.ERR_PARAM
+    assert cs(A, _lib.BF16, 0, ctypes.byref(good), pp, None) == _lib.ERR_SIZE
+    assert cs(A, _lib.BF16, 4096, ctypes.byref(_seg(B, B + 0x10008, B + 0x20000)), pp, None) == _lib.ERR_ALIGN
+    assert cs(A + 8, _lib.BF16, 4096, ctypes.byref(good), pp, None) == _lib.ERR_ALIGN
+    # a segment inside the input, or two segments on top of each other
+    assert cs(A, _lib.BF16, 4096, ctypes.byref(_seg(B, A + 4096, B + 0x20000)), pp, None) == _lib.ERR_OVERLAP
+    assert cs(A, _lib.F32, 4096, ctypes.byref(_seg(B, A + 3 * 4096, B + 0x20000)), pp, None) == _lib.ERR_OVERLAP
+    assert cs(A, _lib.BF16, 4096, ctypes.byref(_seg(B, B + 1024, B + 0x20000)), pp, None) == _lib.ERR_OVERLAP
+    assert cs(A, _lib.BF16, 4096, ctypes.byref(_seg(B, B + 0x10000, B + 0x10000 + 128)), pp, None) == _lib.ERR_OVERLAP
+    assert ds(None, 4096, A, _lib.BF16, 1, pp, None) == _lib.ERR_NULL
+    assert ds(ctypes.byref(good), 4096, A, _lib.BF16, 3, pp, None) == _lib.ERR_PARAM
+    assert ds(ctypes.byref(good), 4096, A + 4, _lib.BF16, 1, pp, None) == _lib.ERR_ALIGN
+    assert ds(ctypes.byref(good), 4096, B + 0x20000 - 64, _lib.BF16, 1, pp, None) == _lib.ERR_OVERLAP
+    two = (_lib.Segments * 2)(_seg(A, A + 0x10000, A + 0x20000), _seg(A + 0x30000, A + 0x40000, A + 0x50000))
+    assert rs(two, 0, 4096, ctypes.byref(good), pp, None) == _lib.ERR_PARAM
+    assert rs(two, 9, 4096, ctypes.byref(good), pp, None) == _lib.ERR_PARAM
+    assert rs(None, 2, 4096, ctypes.byref(good), pp, None) == _lib.ERR_NULL
+    assert rs(two, 2, 4096, None, pp, None) == _lib.ERR_NULL
+    assert rs(two, 2, -5, ctypes.byref(good), pp, None) == _lib.ERR_SIZE
+    assert rs(two, 2, 4096, ctypes.byref(_seg(B + 4, B + 0x10000, B + 0x20000)), pp, None) == _lib.ERR_ALIGN
+    assert rs(two, 2, 4096, ctypes.byref(_seg(A + 0x30000 + 512, B + 0x10000, B + 0x20000)), pp, None) == _lib.ERR_OVERLAP
+    assert rs(two, 2, 4096, ctypes.byref(_seg(B, B + 0x10000, A + 0x40000)), pp, None) == _lib.ERR_OVERLAP
