@@ -102,6 +102,7 @@ def parse(argv=None):
                     "a _mx suffix selects the E8M0 scales")
     ap.add_argument("--n", type=int, default=1 << 26, help="elements for --kernel")
     ap.add_argument("--iters", type=int, default=30, help="timed launches for --kernel")
+    ap.add_argument("--fwht", type=int, default=1, help="transform for --kernel compress (2: tensor-core encoder)")
     return ap.parse_args(argv)
 
 
@@ -577,7 +578,7 @@ def kernel_mode(args):
         nar_y = torch.empty_like(nar)
         nar[:, :1024] = x.view(-1, 1024)
     fns = {
-        "compress": lambda: fq.compress(x, payload=pays[0], scales=sc),
+        "compress": lambda: fq.compress(x, payload=pays[0], scales=sc, fwht=args.fwht),
         "decompress_bf16_b1": lambda: fq.decompress_accumulate(pays[0], n, d16, beta=1, scales=sc),
         "decompress_bf16_b0": lambda: fq.decompress_accumulate(pays[0], n, d16, beta=0, scales=sc),
         "decompress_f32_b1": lambda: fq.decompress_accumulate(pays[0], n, d32, beta=1, scales=sc),
@@ -594,7 +595,8 @@ def kernel_mode(args):
     ms = timer.mean_ms(fn, args.iters)
     require_no_fault(fq, f"--kernel {k}")
     peak, _ = measured_peak()
-    print(json.dumps(kernel_record(base, n, ms, peak, 32 if sc == "e8m0" else 16, sc, variant=k)), flush=True)
+    print(json.dumps(kernel_record(base, n, ms, peak, 32 if sc == "e8m0" else 16, sc, variant=k, fwht=args.fwht)),
+          flush=True)
     return 0
 
 

@@ -1119,6 +1119,8 @@ __device__ __forceinline__ void staging_store(const CUtensorMap* map, const Tile
   tile_store<LPB>(map, T, t, xbuf, lane);
 }
 
+#include "fp4q_tc.cuh"
+
 // K1: compress. x (bfloat16, n) -> payload. Input tiles arrive by TMA.
 // XF: FP32 input (8 KiB tiles of 64 lines) instead of BF16 (4 KiB, 32 lines).
 template <int G, int FWHT, bool MX, bool XF>
@@ -1767,12 +1769,27 @@ bool rows_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The tensor-core compress reads a contiguous BF16 tensor as rows of 16 elements (32 bytes,
+// one group), 128 rows (one 8-block tile) per box, with the 32-byte swizzle its MMA operand
+// layout expects.
+bool group_rows_map(CUtensorMap* m, const void* ptr, int64_t n) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {16, (cuuint64_t)(n / 16)};
+  const cuuint64_t strides[1] = {32};
+  const cuuint32_t box[2] = {16, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 fp4q_status check_params(const fp4q_params* p, int& G, int& fwht, bool& mx) {
   fp4q_params d = {FP4Q_GROUP_DEFAULT, FP4Q_BLOCK, 1, FP4Q_SCALES_DUAL};
   if (p) d = *p;
-  if ((d.group != 16 && d.group != 32) || d.block != FP4Q_BLOCK || (d.fwht != 0 && d.fwht != 1) ||
+  if ((d.group != 16 && d.group != 32) || d.block != FP4Q_BLOCK || d.fwht < 0 || d.fwht > 2 ||
       (d.scales != FP4Q_SCALES_DUAL && d.scales != FP4Q_SCALES_E8M0) ||
-      (d.scales == FP4Q_SCALES_E8M0 && d.group != 32))
+      (d.scales == FP4Q_SCALES_E8M0 && d.group != 32) || (d.fwht == 2 && d.scales != FP4Q_SCALES_DUAL))
     return FP4Q_ERR_PARAM;
   G = d.group;
   fwht = d.fwht;
@@ -1830,6 +1847,29 @@ fp4q_status launch_compress(const void* x, int64_t n, const Payload& P, cudaStre
   if (n == nfull) return FP4Q_OK;
   const void* xt = static_cast<const uint8_t*>(x) + nfull * (XF ? 4 : 2);
   return launch_tail(tail_compress_kernel<G, F, MX, XF>, s, xt, (int)(n - nfull), P, (int64_t)(nfull / FP4Q_BLOCK));
+}
+
+// Tensor-core compress (fwht = 2): full blocks through compress_tc_kernel, persistent, at most
+// kTcCtas CTAs per SM (their TMEM allocations fill the SM's 512 columns); a last partial block
+// through the one-warp tail kernel with the butterfly transform.
+template <int G>
+fp4q_status launch_compress_tc(const void* x, int64_t n, const Payload& P, cudaStream_t s) {
+  const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
+  if (nfull > 0) {
+    const int64_t nb = nfull / FP4Q_BLOCK, tiles = (nb + kTileBlocks - 1) / kTileBlocks;
+    const int64_t batches = (tiles + kTcTiles - 1) / kTcTiles;
+    CUtensorMap xm;
+    if (!group_rows_map(&xm, x, nfull)) return FP4Q_ERR_CUDA;
+    auto k = compress_tc_kernel<G>;
+    Launch L;
+    // plan() sizes the grid as (units / warps) CTAs: 4 units per batch gives one CTA per batch
+    fp4q_status st = plan(k, 4, kTcSmemBytes, 4 * batches, L, kTcCtas);
+    if (st == FP4Q_OK) st = launch_pdl(k, L, 128, s, xm, P, nb, batches);
+    if (st != FP4Q_OK) return st;
+  }
+  if (n == nfull) return FP4Q_OK;
+  const void* xt = static_cast<const uint8_t*>(x) + nfull * 2;
+  return launch_tail(tail_compress_kernel<G, 1, false, false>, s, xt, (int)(n - nfull), P, (int64_t)(nfull / FP4Q_BLOCK));
 }
 
 template <int G, int F, int DT, int B, bool MX>
@@ -1985,6 +2025,10 @@ fp4q_status dispatch_decompress(int key, const Payload& payload, int64_t n, void
 
 template <bool XF>
 fp4q_status dispatch_compress(int G, int F, bool MX, const void* x, int64_t n, const Payload& P, cudaStream_t s) {
+  if (F == 2) {   // tensor-core transform: BF16 input, dual scales (check_params rejects E8M0)
+    if (XF) return FP4Q_ERR_PARAM;
+    return G == 16 ? launch_compress_tc<16>(x, n, P, s) : launch_compress_tc<32>(x, n, P, s);
+  }
   if (MX) return F ? launch_compress<32, 1, true, XF>(x, n, P, s) : launch_compress<32, 0, true, XF>(x, n, P, s);
   if (G == 16) return F ? launch_compress<16, 1, false, XF>(x, n, P, s) : launch_compress<16, 0, false, XF>(x, n, P, s);
   return F ? launch_compress<32, 1, false, XF>(x, n, P, s) : launch_compress<32, 0, false, XF>(x, n, P, s);
@@ -2023,6 +2067,7 @@ fp4q_status roundtrip_entry(const void* x, int64_t n, void* y, const fp4q_params
   bool MX;
   fp4q_status st = check_params(params, G, F, MX);
   if (st != FP4Q_OK) return st;
+  if (F == 2) return FP4Q_ERR_PARAM;   // the tensor-core transform is an encoder option only
   if (!x || !y) return FP4Q_ERR_NULL;
   if (!size_ok(n)) return FP4Q_ERR_SIZE;
   if (!aligned16(x) || !aligned16(y)) return FP4Q_ERR_ALIGN;
@@ -2122,6 +2167,7 @@ fp4q_status fp4q_decompress_accumulate(const void* payload, int64_t n, void* dst
   bool MX;
   fp4q_status st = check_params(params, G, F, MX);
   if (st != FP4Q_OK) return st;
+  if (F == 2) F = 1;   // a tensor-core-encoded payload is decoded like any fwht = 1 payload
   if ((dtype != FP4Q_BF16 && dtype != FP4Q_F32) || (beta != 0 && beta != 1)) return FP4Q_ERR_PARAM;
   if (!payload || !dst) return FP4Q_ERR_NULL;
   if (!size_ok(n)) return FP4Q_ERR_SIZE;
@@ -2148,6 +2194,7 @@ fp4q_status fp4q_compress_2d(const void* x_bf16, int64_t rows, int64_t cols, int
   bool MX;
   fp4q_status st = check_params(params, G, F, MX);
   if (st != FP4Q_OK) return st;
+  if (F == 2) return FP4Q_ERR_PARAM;   // the tensor-core transform takes contiguous input only
   if (!x_bf16 || !payload) return FP4Q_ERR_NULL;
   if ((st = check_2d(rows, cols, ld, 2)) != FP4Q_OK) return st;
   if (!aligned16(x_bf16) || !aligned16(payload)) return FP4Q_ERR_ALIGN;
@@ -2170,6 +2217,7 @@ fp4q_status fp4q_decompress_accumulate_2d(const void* payload, int64_t rows, int
   bool MX;
   fp4q_status st = check_params(params, G, F, MX);
   if (st != FP4Q_OK) return st;
+  if (F == 2) F = 1;   // a tensor-core-encoded payload is decoded like any fwht = 1 payload
   if ((dtype != FP4Q_BF16 && dtype != FP4Q_F32) || (beta != 0 && beta != 1)) return FP4Q_ERR_PARAM;
   if (!payload || !dst) return FP4Q_ERR_NULL;
   const int esz = dtype == FP4Q_BF16 ? 2 : 4;
@@ -2203,6 +2251,7 @@ fp4q_status fp4q_roundtrip_2d(const void* x_bf16, int64_t rows, int64_t cols, in
   bool MX;
   fp4q_status st = check_params(params, G, F, MX);
   if (st != FP4Q_OK) return st;
+  if (F == 2) return FP4Q_ERR_PARAM;   // the tensor-core transform takes contiguous input only
   if (!x_bf16 || !y_bf16) return FP4Q_ERR_NULL;
   if ((st = check_2d(rows, cols, ldx, 2)) != FP4Q_OK || (st = check_2d(rows, cols, ldy, 2)) != FP4Q_OK) return st;
   if (!aligned16(x_bf16) || !aligned16(y_bf16)) return FP4Q_ERR_ALIGN;
@@ -2281,6 +2330,7 @@ fp4q_status fp4q_decompress_accumulate_segments(const fp4q_segments* in, int64_t
   bool MX;
   fp4q_status st = check_params(params, G, F, MX);
   if (st != FP4Q_OK) return st;
+  if (F == 2) F = 1;   // a tensor-core-encoded payload is decoded like any fwht = 1 payload
   if ((dtype != FP4Q_BF16 && dtype != FP4Q_F32) || (beta != 0 && beta != 1)) return FP4Q_ERR_PARAM;
   if (!in || !dst) return FP4Q_ERR_NULL;
   if (!size_ok(n)) return FP4Q_ERR_SIZE;

@@ -1,0 +1,266 @@
+// fp4q_tc.cuh - compress with the transform on the tensor cores (fp4q_params.fwht = 2).
+// Included by fp4q.cu inside its anonymous namespace, after the shared helpers.
+//
+// The method: "FP4Quant" (shd-paper.top), technical framework: a hybrid two-level FWHT in a
+// GPU-aware pipeline. H256 = H16 (x) H16, so y = (1/16) H16 X H16 for a block viewed as the
+// 16 x 16 matrix X[g][p] (g = group, p = position in the group). This encoder evaluates the
+// level that mixes groups as a +-1 matrix product on the 5th-generation tensor cores and the
+// level inside a group in registers:
+//   D = Hbd * Xt    (tcgen05.mma kind::f16, BF16 operands, FP32 accumulation in TMEM)
+// where Xt is the BF16 input of 4 consecutive 8-block tiles exactly as the TMA loads it
+// (rows k = (block, g) of 16 positions, 32-byte swizzle: a K x N = 128 x 64 MN-major operand),
+// and Hbd is the 128 x 128 block-diagonal matrix of eight H16 blocks, applied as eight
+// K = 16 slices (slice j holds H16 in rows 16j .. 16j+15; every slice is a window of one
+// 240-row buffer that has H16 in rows 112 .. 127 and zeros elsewhere). Each TMEM lane then
+// holds one row (block, g') of the group-mixed values for 16 positions; a thread loads it
+// with tcgen05.ld, applies H16 along the positions with FP32 butterflies (one quantisation
+// group per thread) and quantises it as the contract's Scales / Codes / Packing steps do.
+//
+// The products are exact (BF16 times +-1) but the tensor core accumulates the 16 terms of
+// each sum in its own order, and the levels run in the other order than the contract's
+// butterfly sequence, so y matches the contract only to FP32 rounding: scales and codes can
+// differ where the contract's value sits on a rounding boundary. The payload format is the
+// contract's, and every decoder reads it as an fwht = 1 payload.
+//
+// Pipeline (one CTA = one warpgroup, persistent over batches of 4 tiles): thread 0 keeps two
+// batches of input in flight by TMA, issues the eight MMAs of the next batch into the second
+// TMEM accumulator while the warpgroup reads and quantises the current one, and refills a
+// stage as soon as the MMAs that read it have completed (tcgen05.commit -> mbarrier). Every
+// wait is bounded; a wait that gives up sets the fault word, the CTA drains what it issued
+// (bounded) and frees its TMEM.
+
+constexpr int kTcTiles = 4;                          // 8-block tiles per batch (MMA N = 64)
+constexpr int kTcStages = 2;                         // input batches in flight per CTA
+constexpr int kTcBatchBytes = kTcTiles * 4096;       // BF16 input of one batch
+constexpr int kTcZBytes = 8192;                      // A operand buffer (240 rows used)
+constexpr int kTcAccCols = 16 * kTcTiles;            // TMEM columns of one FP32 accumulator
+constexpr uint32_t kTcTmemCols = 2 * kTcAccCols;     // two accumulators (a power of two >= 32)
+constexpr int kTcCtas = 4;                           // resident CTAs per SM: 512 TMEM columns / 128
+constexpr int kTcSmemBytes = 1024 + kTcZBytes + kTcStages * kTcBatchBytes;
+
+// Shared-memory matrix descriptor of tcgen05.mma: start address, leading and stride byte
+// offsets (16-byte units), the sm_100 descriptor version (bit 46) and the swizzle mode.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | (uint64_t)((lbo >> 4) & 0x3FFFu) << 16 |
+         (uint64_t)((sbo >> 4) & 0x3FFFu) << 32 | (uint64_t)1 << 46 | (uint64_t)swizzle << 61;
+}
+constexpr uint32_t kUmmaSwizzle32B = 6;
+// Instruction descriptor (kind::f16): D FP32, A and B BF16, A K-major, B MN-major,
+// N = kTcAccCols, M = 128.
+constexpr uint32_t kTcIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                              ((uint32_t)(kTcAccCols >> 3) << 17) | ((128u >> 4) << 24);
+// Operand layouts (checked on the hardware against a CPU product): A K-major without swizzle,
+// core matrices of 8 rows x 16 bytes, K-group stride 128 bytes (LBO), row-group stride 256
+// (SBO); B MN-major with the 32-byte swizzle the TMA writes, 16-column group stride 4096 bytes
+// (one tile; LBO), 8-row group stride 256 bytes (SBO).
+constexpr uint32_t kTcALbo = 128, kTcASbo = 256, kTcBLbo = 4096, kTcBSbo = 256;
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+               ::"r"(d_tmem), "l"(a), "l"(b), "r"(kTcIdesc), "r"(accumulate)
+               : "memory");
+}
+// Arrive on an mbarrier once every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 16 consecutive 32-bit TMEM columns of the warp's 32 lanes (one row per thread).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 v[8]) {
+  uint32_t r[16];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+               "tcgen05.wait::ld.sync.aligned;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+}
+
+// Quantised row: the 16 codes of one group row, its group-scale code and the block scale.
+struct RowQ {
+  uint32_t w0, w1, sg;
+  float sb;
+};
+
+// Dual-scale quantisation of one 16-element row per thread; the 16 lanes of a half-warp hold
+// the 16 rows of one block. v is the unnormalised transform z = 16 y (the scales fold the
+// 1/16 as the tiled kernels do).
+template <int G>
+__device__ __forceinline__ void quantize_row(const float2 v[8], RowQ& o) {
+  float a[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    a[2 * j] = fabsf(v[j].x);
+    a[2 * j + 1] = fabsf(v[j].y);
+  }
+  const float m0 = max3(a[0], a[1], a[2]), m1 = max3(a[3], a[4], a[5]), m2 = max3(a[6], a[7], a[8]);
+  const float m3 = max3(a[9], a[10], a[11]), m4 = max3(a[12], a[13], a[14]);
+  float am = max3(max3(m0, m1, m2), fmaxf(m3, m4), a[15]);
+  float A = am;
+#pragma unroll
+  for (int k = 1; k < 16; k <<= 1) A = fmaxf(A, __shfl_xor_sync(kFull, A, k));
+  if (G == 32) am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));
+  A = __fmul_rn(A, 0.0625f);
+  am = __fmul_rn(am, 0.0625f);
+  const bool zero = !(A >= kZeroLimit);
+  const float sb = zero ? 0.0f : fp4q_math::div_rn_2688(A);
+  const float tb = zero ? 1.0f : __fmul_rn(sb, 6.0f);
+  const fp4q_math::Divider by_tb(tb);
+  uint32_t c = e4m3x2(by_tb.div(am), 0.0f) & 0xffu;
+  if (zero) c = 0u;
+  const float S = __fmul_rn(e4m3x2_to_f2(c).x, sb);
+  float inv = S > 0.0f ? fp4q_math::rcp_rn(S) : 0.0f;
+  inv = __fmul_rn(inv, 0.0625f);
+  const float2 iv = make_float2(inv, inv);
+  uint32_t w0 = e2m1_pack8(mul2(v[0], iv), mul2(v[1], iv), mul2(v[2], iv), mul2(v[3], iv));
+  uint32_t w1 = e2m1_pack8(mul2(v[4], iv), mul2(v[5], iv), mul2(v[6], iv), mul2(v[7], iv));
+  if (zero) w0 = w1 = 0u;
+  o.w0 = w0;
+  o.w1 = w1;
+  o.sg = c;
+  o.sb = sb;
+}
+
+// Store one row (group row g of block gb): 8 bytes of codes, its group-scale byte (G = 16;
+// for G = 32 the even row of the pair), the block scale from row 0.
+template <int G>
+__device__ __forceinline__ void store_row(const Payload& P, int64_t gb, int g, const RowQ& q) {
+  *reinterpret_cast<uint2*>(P.codes + gb * 128 + g * 8) = make_uint2(q.w0, q.w1);
+  if (G == 16) {
+    P.gsc[gb * 16 + g] = (uint8_t)q.sg;
+  } else if (!(g & 1)) {
+    P.gsc[gb * 8 + (g >> 1)] = (uint8_t)q.sg;
+  }
+  if (g == 0) {
+    P.bsc[gb] = q.sb;
+    if (G == 32 && (P.nb & 1) && gb == P.nb - 1) *reinterpret_cast<uint2*>(P.gsc + 8 * P.nb) = make_uint2(0u, 0u);
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(128, kTcCtas)
+compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t nb, int64_t batches) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kTcStages + 2];   // input stages full, accumulators done
+  __shared__ uint32_t tmem_slot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t zbuf = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  const uint32_t stage0 = zbuf + kTcZBytes;
+  const uint32_t full0 = smem_addr(&bars[0]), done0 = smem_addr(&bars[kTcStages]);
+  const int64_t tiles = (nb + kTileBlocks - 1) / kTileBlocks;
+
+  // A operand: row r, column k at (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2;
+  // rows 112 .. 127 hold H16 (entry (i, k) = (-1)^popcount(i & k), exact in BF16), the rest 0.
+  for (int u = tid; u < kTcZBytes / 16; u += 128) {
+    const int r = 8 * (u >> 4) + (u & 7), k0 = 8 * ((u >> 3) & 1);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (r >= 112 && r < 128) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t h = (__popc((uint32_t)((r - 112) & (k0 + e))) & 1) ? 0xBF80u : 0x3F80u;
+        w[e >> 1] |= h << (16 * (e & 1));
+      }
+    }
+    sts128(zbuf + 16u * (uint32_t)u, make_uint4(w[0], w[1], w[2], w[3]));
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kTcStages + 2; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_slot)),
+                 "r"(kTcTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_proxy_async();                       // the A operand, written by threads, read by the MMA
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  const int64_t first = blockIdx.x, step = gridDim.x;
+  const int64_t mine = first < batches ? (batches - 1 - first) / step + 1 : 0;
+  int64_t loaded = 0, issued = 0;            // thread 0: batches loaded by TMA / with MMAs issued
+  auto load = [&](int64_t i) {
+    const int64_t t0 = (first + i * step) * kTcTiles;
+    const int nt = (int)(tiles - t0 < kTcTiles ? tiles - t0 : kTcTiles);
+    const uint32_t st = stage0 + (uint32_t)((i % kTcStages) * kTcBatchBytes), bar = full0 + 8u * (uint32_t)(i % kTcStages);
+    mbar_expect_tx(bar, (uint32_t)nt * 4096u);
+    for (int t = 0; t < nt; ++t) tma_load_2d(st + 4096u * (uint32_t)t, &xmap, 0, (int32_t)((t0 + t) * 128), bar);
+    ++loaded;
+  };
+  auto mma = [&](int64_t i) -> bool {
+    if (!mbar_wait(full0 + 8u * (uint32_t)(i % kTcStages), (uint32_t)((i / kTcStages) & 1), kSpinLimit)) return false;
+    tc_fence_after();
+    const uint32_t st = stage0 + (uint32_t)((i % kTcStages) * kTcBatchBytes);
+    const uint32_t d = tmem + (uint32_t)((i & 1) * kTcAccCols);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      umma_bf16(d, umma_desc(zbuf + (uint32_t)(14 - 2 * j) * 256u, kTcALbo, kTcASbo, 0),
+                umma_desc(st + 512u * (uint32_t)j, kTcBLbo, kTcBSbo, kUmmaSwizzle32B), j > 0);
+    umma_commit(done0 + 8u * (uint32_t)(i & 1));
+    ++issued;
+    return true;
+  };
+  bool fail = false;
+  if (tid == 0) {
+    for (int64_t i = 0; i < kTcStages && i < mine; ++i) load(i);
+    if (mine > 0) fail = !mma(0);
+  }
+  const int row = warp * 32 + lane, g = lane & 15;
+  int64_t i = 0;
+  for (; i < mine; ++i) {
+    if (tid == 0 && !fail && i + 1 < mine) {
+      tc_fence_after();
+      fail = !mma(i + 1);                    // the next batch's products while this one is read
+    }
+    // warp-uniform, as the .sync.aligned TMEM loads below require
+    const bool ok = __all_sync(kFull, mbar_wait(done0 + 8u * (uint32_t)(i & 1), (uint32_t)((i >> 1) & 1), kSpinLimit));
+    tc_fence_after();
+    if (tid == 0 && ok && !fail && i + kTcStages < mine) load(i + kTcStages);   // MMAs of batch i read that stage
+    if (ok) {
+      const uint32_t acc = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)((i & 1) * kTcAccCols);
+      const int64_t t0 = (first + i * step) * kTcTiles;
+#pragma unroll 1
+      for (int t = 0; t < kTcTiles; ++t) {
+        if (t0 + t >= tiles) break;          // uniform over the CTA
+        float2 v[8];
+        tmem_ld16(acc + 16u * (uint32_t)t, v);
+        // the level inside a group: H16 along the 16 positions (strides 1, 2, 4, 8)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) bfly_in(v[j]);
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (!(j & h)) bfly2(v[j], v[j + h]);
+        RowQ q;
+        quantize_row<G>(v, q);
+        const int64_t gb = (t0 + t) * kTileBlocks + (row >> 4);
+        if (gb < nb) store_row<G>(P, gb, g, q);
+      }
+    }
+    tc_fence_before();
+    if (__syncthreads_or(fail || !ok)) break;
+  }
+  if (i < mine && tid == 0) {
+    // gave up a wait: record it, then wait (bounded) for what is still in flight
+    atomicOr(&g_fp4q_fault, kFaultLoadWait);
+    for (int64_t k = issued; k < loaded; ++k)
+      if (!mbar_wait(full0 + 8u * (uint32_t)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), kSpinLimit))
+        atomicOr(&g_fp4q_fault, kFaultDrainWait);
+    for (int64_t k = i; k < issued; ++k)
+      if (!mbar_wait(done0 + 8u * (uint32_t)(k & 1), (uint32_t)((k >> 1) & 1), kSpinLimit))
+        atomicOr(&g_fp4q_fault, kFaultDrainWait);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols) : "memory");
+}

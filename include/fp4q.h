@@ -65,6 +65,17 @@
  *   Reduce.  z = x~_0 + x~_1 + ... + x~_{R-1} (FP32, in rank order, no FMA), decoded in
  *            the transform domain (no inverse FWHT), then Scales/Codes/Packing on z with
  *            no forward FWHT. [P3 "Read it as": the AllReduce of tensor parallelism]
+ *   Tensor-core encoder (fwht = 2; relaxed, opt-in) [P1 "hybrid two-level FWHT pipeline",
+ *            "GPU-aware execution optimization"]: the same y = H256 x / 16, with the level
+ *            that mixes the 16 groups of a block computed first, as a +-1 BF16 matrix product
+ *            on the tensor cores (exact products, FP32 accumulation in the hardware's order),
+ *            then the level inside each group as FP32 butterflies. y agrees with the FWHT
+ *            step above to FP32 rounding only (about 1e-6 of the block maximum), so a scale
+ *            or a code whose contract value lies on a rounding boundary can differ; the
+ *            payload format is unchanged and decodes as an fwht = 1 payload. Contiguous
+ *            BF16 input and dual scales only (fp4q_compress, fp4q_compress_segments); the
+ *            decoders and the reduce accept fwht = 2 as fwht = 1; the other producers reject
+ *            it (FP4Q_ERR_PARAM).
  *
  * Every floating-point step is a separately rounded FP32 operation (no FMA contraction),
  * so the GPU result is bit-identical to a plain scalar evaluation of the steps above.
@@ -114,8 +125,8 @@ typedef enum fp4q_status {
   FP4Q_ERR_NULL = 1,     /* a required pointer is NULL                                  */
   FP4Q_ERR_SIZE = 2,     /* n <= 0 or n >= 2^37                                         */
   FP4Q_ERR_ALIGN = 3,    /* a data pointer is not 16-byte aligned                       */
-  FP4Q_ERR_PARAM = 4,    /* bad params: group not 16/32, block not 256, fwht not 0/1,
-                            scales not 0/1 or E8M0 with group != 32, R outside [1, 8],
+  FP4Q_ERR_PARAM = 4,    /* bad params: group not 16/32, block not 256, fwht not 0/1/2,
+                            scales not 0/1, E8M0 with group != 32 or fwht 2, R outside [1, 8],
                             unknown dtype, beta not 0/1                                 */
   FP4Q_ERR_OVERLAP = 5,  /* an output buffer overlaps an input buffer                   */
   FP4Q_ERR_CUDA = 6      /* a CUDA runtime call or a kernel launch failed               */
@@ -124,7 +135,8 @@ typedef enum fp4q_status {
 typedef struct fp4q_params {
   int32_t group;  /* G: 16 (default) or 32 elements per group scale                    */
   int32_t block;  /* must be 256                                                        */
-  int32_t fwht;   /* 1: apply the FWHT (default); 0: quantize the raw values            */
+  int32_t fwht;   /* 1: apply the FWHT (default); 0: quantize the raw values; 2: the FWHT
+                     with the tensor-core encoder (relaxed; see above)                     */
   int32_t scales; /* FP4Q_SCALES_DUAL (default) or FP4Q_SCALES_E8M0 (needs group 32)    */
 } fp4q_params;
 
