@@ -1849,9 +1849,9 @@ fp4q_status launch_compress(const void* x, int64_t n, const Payload& P, cudaStre
   return launch_tail(tail_compress_kernel<G, F, MX, XF>, s, xt, (int)(n - nfull), P, (int64_t)(nfull / FP4Q_BLOCK));
 }
 
-// Tensor-core compress (fwht = 2): full blocks through compress_tc_kernel, persistent, at most
-// kTcCtas CTAs per SM (their TMEM allocations fill the SM's 512 columns); a last partial block
-// through the one-warp tail kernel with the butterfly transform.
+// Tensor-core compress (fwht = 2): full blocks through compress_tc_kernel, persistent, one CTA
+// per SM (its TMEM allocation is the SM's 512 columns); a last partial block through the
+// one-warp tail kernel with the butterfly transform.
 template <int G>
 fp4q_status launch_compress_tc(const void* x, int64_t n, const Payload& P, cudaStream_t s) {
   const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
@@ -1862,9 +1862,11 @@ fp4q_status launch_compress_tc(const void* x, int64_t n, const Payload& P, cudaS
     if (!group_rows_map(&xm, x, nfull)) return FP4Q_ERR_CUDA;
     auto k = compress_tc_kernel<G>;
     Launch L;
-    // plan() sizes the grid as (units / warps) CTAs: 4 units per batch gives one CTA per batch
-    fp4q_status st = plan(k, 4, kTcSmemBytes, 4 * batches, L, kTcCtas);
-    if (st == FP4Q_OK) st = launch_pdl(k, L, 128, s, xm, P, nb, batches);
+    // plan() sizes the grid as (units / warps) CTAs: one unit per warp and batch gives one CTA
+    // per batch, capped at one per SM
+    constexpr int warps = kTcThreads / 32;
+    fp4q_status st = plan(k, warps, kTcSmemBytes, warps * batches, L, 1);
+    if (st == FP4Q_OK) st = launch_pdl(k, L, kTcThreads, s, xm, P, nb, batches);
     if (st != FP4Q_OK) return st;
   }
   if (n == nfull) return FP4Q_OK;

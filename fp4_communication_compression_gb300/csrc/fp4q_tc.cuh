@@ -22,20 +22,26 @@
 // differ where the contract's value sits on a rounding boundary. The payload format is the
 // contract's, and every decoder reads it as an fwht = 1 payload.
 //
-// Pipeline (one CTA = one warpgroup, persistent over batches of 4 tiles): thread 0 keeps two
-// batches of input in flight by TMA, issues the eight MMAs of the next batch into the second
-// TMEM accumulator while the warpgroup reads and quantises the current one, and refills a
-// stage as soon as the MMAs that read it have completed (tcgen05.commit -> mbarrier). Every
-// wait is bounded; a wait that gives up sets the fault word, the CTA drains what it issued
-// (bounded) and frees its TMEM.
+// Pipeline (warp-specialised, one persistent CTA per SM): a producer warp keeps up to
+// kTcStages - 1 batches of 4 tiles ahead in flight by TMA and issues the eight MMAs of each
+// batch as soon as its input has landed and its TMEM accumulator is free; kTcGroups consumer
+// warpgroups take the batches in turn, each with its own pair of accumulators: a consumer
+// copies an accumulator to registers (one tcgen05.ld of 64 columns), frees it at once, then
+// applies the in-group level and quantises while the tensor cores fill the next one. MMA
+// completion is signalled with tcgen05.commit to mbarriers (accumulator full, input stage
+// free). Every wait is bounded; a wait that gives up sets the fault word and a CTA-wide stop
+// flag, the producer waits (bounded) for the copies and products it issued, and the CTA frees
+// its TMEM.
 
 constexpr int kTcTiles = 4;                          // 8-block tiles per batch (MMA N = 64)
-constexpr int kTcStages = 2;                         // input batches in flight per CTA
+constexpr int kTcGroups = 4;                         // consumer warpgroups
+constexpr int kTcAcc = 2 * kTcGroups;                // TMEM accumulators (two per warpgroup)
+constexpr int kTcStages = 8;                         // input batches buffered per CTA
 constexpr int kTcBatchBytes = kTcTiles * 4096;       // BF16 input of one batch
 constexpr int kTcZBytes = 8192;                      // A operand buffer (240 rows used)
 constexpr int kTcAccCols = 16 * kTcTiles;            // TMEM columns of one FP32 accumulator
-constexpr uint32_t kTcTmemCols = 2 * kTcAccCols;     // two accumulators (a power of two >= 32)
-constexpr int kTcCtas = 4;                           // resident CTAs per SM: 512 TMEM columns / 128
+constexpr uint32_t kTcTmemCols = kTcAcc * kTcAccCols;  // 512: the whole TMEM of the SM
+constexpr int kTcThreads = 32 * (4 * kTcGroups + 1);   // consumers + one producer warp
 constexpr int kTcSmemBytes = 1024 + kTcZBytes + kTcStages * kTcBatchBytes;
 
 // Shared-memory matrix descriptor of tcgen05.mma: start address, leading and stride byte
@@ -67,18 +73,16 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-// 16 consecutive 32-bit TMEM columns of the warp's 32 lanes (one row per thread).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 v[8]) {
-  uint32_t r[16];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-               "tcgen05.wait::ld.sync.aligned;"
+// 16 consecutive 32-bit TMEM columns of the warp's 32 lanes (one row per thread), without
+// waiting: the registers are valid after tmem_ld_wait.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t r[16]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
                  "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                : "r"(taddr)
                : "memory");
-#pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
 }
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Quantised row: the 16 codes of one group row, its group-scale code and the block scale.
 struct RowQ {
@@ -141,21 +145,35 @@ __device__ __forceinline__ void store_row(const Payload& P, int64_t gb, int g, c
   }
 }
 
+// One poll loop of the pipeline: bounded, and it also gives up when another thread of the CTA
+// has already given up (stop flag in shared memory).
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, const volatile uint32_t* stop) {
+  for (uint32_t k = 0; k < kSpinLimit; ++k) {
+    if (mbar_try_wait(bar, parity, kSuspendHintNs)) return true;
+    if ((k & 63u) == 63u && *stop) return false;
+  }
+  return false;
+}
+
 template <int G>
-__global__ void __launch_bounds__(128, kTcCtas)
+__global__ void __launch_bounds__(kTcThreads, 1)
 compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t nb, int64_t batches) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[kTcStages + 2];   // input stages full, accumulators done
+  // mbarriers: input stage full (TMA), input stage free (MMA done), accumulator full (MMA done),
+  // accumulator free (its 4 consumer warps have read it)
+  __shared__ __align__(8) uint64_t bars[2 * kTcStages + 2 * kTcAcc];
   __shared__ uint32_t tmem_slot;
+  __shared__ volatile uint32_t stop;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t zbuf = (smem_addr(smem_raw) + 1023u) & ~1023u;
   const uint32_t stage0 = zbuf + kTcZBytes;
-  const uint32_t full0 = smem_addr(&bars[0]), done0 = smem_addr(&bars[kTcStages]);
+  const uint32_t full0 = smem_addr(&bars[0]), sfree0 = full0 + 8u * kTcStages;
+  const uint32_t afull0 = sfree0 + 8u * kTcStages, afree0 = afull0 + 8u * kTcAcc;
   const int64_t tiles = (nb + kTileBlocks - 1) / kTileBlocks;
 
   // A operand: row r, column k at (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2;
   // rows 112 .. 127 hold H16 (entry (i, k) = (-1)^popcount(i & k), exact in BF16), the rest 0.
-  for (int u = tid; u < kTcZBytes / 16; u += 128) {
+  for (int u = tid; u < kTcZBytes / 16; u += kTcThreads) {
     const int r = 8 * (u >> 4) + (u & 7), k0 = 8 * ((u >> 3) & 1);
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     if (r >= 112 && r < 128) {
@@ -168,7 +186,15 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
     sts128(zbuf + 16u * (uint32_t)u, make_uint4(w[0], w[1], w[2], w[3]));
   }
   if (tid == 0) {
-    for (int s = 0; s < kTcStages + 2; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(sfree0 + 8u * s, 1);
+    }
+    for (int a = 0; a < kTcAcc; ++a) {
+      mbar_init(afull0 + 8u * a, 1);
+      mbar_init(afree0 + 8u * a, 4);
+    }
+    stop = 0u;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -186,52 +212,88 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
 
   const int64_t first = blockIdx.x, step = gridDim.x;
   const int64_t mine = first < batches ? (batches - 1 - first) / step + 1 : 0;
-  int64_t loaded = 0, issued = 0;            // thread 0: batches loaded by TMA / with MMAs issued
-  auto load = [&](int64_t i) {
-    const int64_t t0 = (first + i * step) * kTcTiles;
-    const int nt = (int)(tiles - t0 < kTcTiles ? tiles - t0 : kTcTiles);
-    const uint32_t st = stage0 + (uint32_t)((i % kTcStages) * kTcBatchBytes), bar = full0 + 8u * (uint32_t)(i % kTcStages);
-    mbar_expect_tx(bar, (uint32_t)nt * 4096u);
-    for (int t = 0; t < nt; ++t) tma_load_2d(st + 4096u * (uint32_t)t, &xmap, 0, (int32_t)((t0 + t) * 128), bar);
-    ++loaded;
-  };
-  auto mma = [&](int64_t i) -> bool {
-    if (!mbar_wait(full0 + 8u * (uint32_t)(i % kTcStages), (uint32_t)((i / kTcStages) & 1), kSpinLimit)) return false;
-    tc_fence_after();
-    const uint32_t st = stage0 + (uint32_t)((i % kTcStages) * kTcBatchBytes);
-    const uint32_t d = tmem + (uint32_t)((i & 1) * kTcAccCols);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      umma_bf16(d, umma_desc(zbuf + (uint32_t)(14 - 2 * j) * 256u, kTcALbo, kTcASbo, 0),
-                umma_desc(st + 512u * (uint32_t)j, kTcBLbo, kTcBSbo, kUmmaSwizzle32B), j > 0);
-    umma_commit(done0 + 8u * (uint32_t)(i & 1));
-    ++issued;
-    return true;
-  };
-  bool fail = false;
-  if (tid == 0) {
-    for (int64_t i = 0; i < kTcStages && i < mine; ++i) load(i);
-    if (mine > 0) fail = !mma(0);
-  }
-  const int row = warp * 32 + lane, g = lane & 15;
-  int64_t i = 0;
-  for (; i < mine; ++i) {
-    if (tid == 0 && !fail && i + 1 < mine) {
-      tc_fence_after();
-      fail = !mma(i + 1);                    // the next batch's products while this one is read
-    }
-    // warp-uniform, as the .sync.aligned TMEM loads below require
-    const bool ok = __all_sync(kFull, mbar_wait(done0 + 8u * (uint32_t)(i & 1), (uint32_t)((i >> 1) & 1), kSpinLimit));
-    tc_fence_after();
-    if (tid == 0 && ok && !fail && i + kTcStages < mine) load(i + kTcStages);   // MMAs of batch i read that stage
-    if (ok) {
-      const uint32_t acc = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)((i & 1) * kTcAccCols);
+  if (warp == 4 * kTcGroups) {
+    // ---------------------------------------------------------------- producer warp
+    int64_t loaded = 0, issued = 0;
+    bool ok = true;
+    auto load = [&](int64_t i) {               // lane 0: TMA of batch i into stage i % kTcStages
       const int64_t t0 = (first + i * step) * kTcTiles;
-#pragma unroll 1
+      const int nt = (int)(tiles - t0 < kTcTiles ? tiles - t0 : kTcTiles);
+      const uint32_t st = stage0 + (uint32_t)((i % kTcStages) * kTcBatchBytes), bar = full0 + 8u * (uint32_t)(i % kTcStages);
+      if (lane == 0) {
+        mbar_expect_tx(bar, (uint32_t)nt * 4096u);
+        for (int t = 0; t < nt; ++t) tma_load_2d(st + 4096u * (uint32_t)t, &xmap, 0, (int32_t)((t0 + t) * 128), bar);
+      }
+    };
+    for (; loaded < kTcStages - 1 && loaded < mine; ++loaded) load(loaded);
+    for (int64_t i = 0; i < mine && ok; ++i) {
+      const int s = (int)(i % kTcStages), a = (int)(i % kTcAcc);
+      ok = __all_sync(kFull, tc_wait(full0 + 8u * s, (uint32_t)((i / kTcStages) & 1), &stop));
+      if (ok && i >= kTcAcc) ok = __all_sync(kFull, tc_wait(afree0 + 8u * a, (uint32_t)(((i / kTcAcc) - 1) & 1), &stop));
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t st = stage0 + (uint32_t)(s * kTcBatchBytes), d = tmem + (uint32_t)(a * kTcAccCols);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          umma_bf16(d, umma_desc(zbuf + (uint32_t)(14 - 2 * j) * 256u, kTcALbo, kTcASbo, 0),
+                    umma_desc(st + 512u * (uint32_t)j, kTcBLbo, kTcBSbo, kUmmaSwizzle32B), j > 0);
+        umma_commit(afull0 + 8u * a);
+        umma_commit(sfree0 + 8u * s);
+      }
+      __syncwarp();
+      issued = i + 1;
+      // refill the stage batch i - 1 used, once its products are done
+      if (loaded < mine && i >= 1) {
+        const int64_t k = i - 1;
+        ok = __all_sync(kFull, tc_wait(sfree0 + 8u * (uint32_t)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), &stop));
+        if (!ok) break;
+        load(loaded++);
+      } else if (loaded < mine) {
+        load(loaded++);                        // i == 0: the last free stage
+      }
+    }
+    if (!ok) {
+      if (lane == 0) {
+        stop = 1u;
+        atomicOr(&g_fp4q_fault, kFaultLoadWait);
+      }
+      // wait (bounded) for the copies and products still in flight before the TMEM is freed
+      for (int64_t k = issued; k < loaded; ++k)
+        if (!mbar_wait(full0 + 8u * (uint32_t)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), kSpinLimit) && lane == 0)
+          atomicOr(&g_fp4q_fault, kFaultDrainWait);
+      for (int64_t k = issued > kTcStages ? issued - kTcStages : 0; k < issued; ++k)
+        if (!mbar_wait(sfree0 + 8u * (uint32_t)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), kSpinLimit) && lane == 0)
+          atomicOr(&g_fp4q_fault, kFaultDrainWait);
+    }
+  } else {
+    // ---------------------------------------------------------------- consumer warpgroups
+    const int grp = warp >> 2, wq = warp & 3;   // warpgroup, and its quarter of the TMEM lanes
+    const int row = wq * 32 + lane, g = lane & 15;
+    for (int64_t i = grp; i < mine; i += kTcGroups) {
+      const int a = (int)(i % kTcAcc);
+      if (!__all_sync(kFull, tc_wait(afull0 + 8u * a, (uint32_t)((i / kTcAcc) & 1), &stop))) {
+        if (lane == 0) {
+          stop = 1u;
+          atomicOr(&g_fp4q_fault, kFaultLoadWait);
+        }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t acc = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * kTcAccCols);
+      uint32_t r[kTcTiles][16];
+#pragma unroll
+      for (int t = 0; t < kTcTiles; ++t) tmem_ld16(acc + 16u * (uint32_t)t, r[t]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(afree0 + 8u * a) : "memory");
+      const int64_t t0 = (first + i * step) * kTcTiles;
+#pragma unroll
       for (int t = 0; t < kTcTiles; ++t) {
-        if (t0 + t >= tiles) break;          // uniform over the CTA
         float2 v[8];
-        tmem_ld16(acc + 16u * (uint32_t)t, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = make_float2(__uint_as_float(r[t][2 * j]), __uint_as_float(r[t][2 * j + 1]));
         // the level inside a group: H16 along the 16 positions (strides 1, 2, 4, 8)
 #pragma unroll
         for (int j = 0; j < 8; ++j) bfly_in(v[j]);
@@ -243,21 +305,9 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
         RowQ q;
         quantize_row<G>(v, q);
         const int64_t gb = (t0 + t) * kTileBlocks + (row >> 4);
-        if (gb < nb) store_row<G>(P, gb, g, q);
+        if (t0 + t < tiles && gb < nb) store_row<G>(P, gb, g, q);
       }
     }
-    tc_fence_before();
-    if (__syncthreads_or(fail || !ok)) break;
-  }
-  if (i < mine && tid == 0) {
-    // gave up a wait: record it, then wait (bounded) for what is still in flight
-    atomicOr(&g_fp4q_fault, kFaultLoadWait);
-    for (int64_t k = issued; k < loaded; ++k)
-      if (!mbar_wait(full0 + 8u * (uint32_t)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), kSpinLimit))
-        atomicOr(&g_fp4q_fault, kFaultDrainWait);
-    for (int64_t k = i; k < issued; ++k)
-      if (!mbar_wait(done0 + 8u * (uint32_t)(k & 1), (uint32_t)((k >> 1) & 1), kSpinLimit))
-        atomicOr(&g_fp4q_fault, kFaultDrainWait);
   }
   tc_fence_before();
   __syncthreads();

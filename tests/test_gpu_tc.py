@@ -140,9 +140,12 @@ def test_guard_bands_and_segments(dev):
 
 def test_unsupported_combinations_rejected(dev):
     x = inputs.bits_to_torch(inputs.sweep(4096), dev)
-    with pytest.raises(fq.Fp4qError) as e:
+    with pytest.raises(ValueError):                  # no payload size for this format
         fq.compress(x, fwht=2, scales="e8m0")
-    assert e.value.status == _lib.ERR_PARAM
+    p = torch.empty(fq.payload_bytes(4096, 32), dtype=torch.uint8, device=dev)
+    st = _lib.lib().fp4q_compress(ctypes.c_void_p(x.data_ptr()), 4096, ctypes.c_void_p(p.data_ptr()),
+                                  ctypes.byref(_lib.Params(32, 256, 2, 1)), None)
+    assert st == _lib.ERR_PARAM
     with pytest.raises(fq.Fp4qError):
         fq.roundtrip(x, fwht=2)
     with pytest.raises(fq.Fp4qError):
