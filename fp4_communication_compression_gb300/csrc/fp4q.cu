@@ -687,17 +687,26 @@ __device__ __forceinline__ void fence_proxy_async() {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-// One bounded poll of a barrier phase; the thread may be suspended up to hint_ns.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+// One poll of a barrier phase. Without a suspend-time hint the hardware holds the thread for at
+// most a short, implementation-defined window while the phase is incomplete; with a hint
+// (an earlier version passed 1000 ns) a wait that was entered a little early could sleep
+// well past the phase's completion.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "r"(bar), "r"(parity)
       : "memory");
   return done != 0;
+}
+// Nanoseconds of the GPU's global timer (used only to bound waits).
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
                                             uint32_t bar) {
@@ -746,13 +755,18 @@ constexpr unsigned kFaultLoadWait = 1u;    // a TMA load did not complete within
 constexpr unsigned kFaultDrainWait = 2u;   // a copy still in flight after a fault did not complete
 constexpr unsigned kFaultSelftest = 4u;    // the self-test wait ran out (expected)
 
-// A wait is declared failed after kSpinLimit polls of at most kSuspendHintNs each (~1 s).
-constexpr uint32_t kSpinLimit = 1u << 20;
-constexpr uint32_t kSuspendHintNs = 1000;
+// A wait is declared failed after kWaitLimitNs of the global timer (about a second) or after
+// its poll budget, whichever comes first.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr uint32_t kSpinLimit = 1u << 30;
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t polls) {
-  for (uint32_t i = 0; i < polls; ++i)
-    if (mbar_try_wait(bar, parity, kSuspendHintNs)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1; i < polls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0u && global_ns() - t0 > kWaitLimitNs) return false;
+  }
   return false;
 }
 

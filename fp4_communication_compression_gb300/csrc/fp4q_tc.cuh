@@ -22,8 +22,8 @@
 // differ where the contract's value sits on a rounding boundary. The payload format is the
 // contract's, and every decoder reads it as an fwht = 1 payload.
 //
-// Pipeline (warp-specialised, one persistent CTA per SM): a producer warp keeps up to
-// kTcStages - 1 batches of 4 tiles ahead in flight by TMA and issues the eight MMAs of each
+// Pipeline (warp-specialised, one persistent CTA per SM): a producer warp keeps
+// kTcStages - kTcRefillLag batches of 4 tiles ahead in flight by TMA and issues the eight MMAs of each
 // batch as soon as its input has landed and its TMEM accumulator is free; kTcGroups consumer
 // warpgroups take the batches in turn, each with its own pair of accumulators: a consumer
 // copies an accumulator to registers (one tcgen05.ld of 64 columns), frees it at once, then
@@ -37,6 +37,7 @@ constexpr int kTcTiles = 4;                          // 8-block tiles per batch 
 constexpr int kTcGroups = 4;                         // consumer warpgroups
 constexpr int kTcAcc = 2 * kTcGroups;                // TMEM accumulators (two per warpgroup)
 constexpr int kTcStages = 8;                         // input batches buffered per CTA
+constexpr int kTcRefillLag = 2;                      // a stage is refilled this many batches after its MMAs
 constexpr int kTcBatchBytes = kTcTiles * 4096;       // BF16 input of one batch
 constexpr int kTcZBytes = 8192;                      // A operand buffer (240 rows used)
 constexpr int kTcAccCols = 16 * kTcTiles;            // TMEM columns of one FP32 accumulator
@@ -148,9 +149,11 @@ __device__ __forceinline__ void store_row(const Payload& P, int64_t gb, int g, c
 // One poll loop of the pipeline: bounded, and it also gives up when another thread of the CTA
 // has already given up (stop flag in shared memory).
 __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, const volatile uint32_t* stop) {
-  for (uint32_t k = 0; k < kSpinLimit; ++k) {
-    if (mbar_try_wait(bar, parity, kSuspendHintNs)) return true;
-    if ((k & 63u) == 63u && *stop) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t k = 1; k < kSpinLimit; ++k) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((k & 63u) == 0u && (*stop || global_ns() - t0 > kWaitLimitNs)) return false;
   }
   return false;
 }
@@ -225,7 +228,7 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
         for (int t = 0; t < nt; ++t) tma_load_2d(st + 4096u * (uint32_t)t, &xmap, 0, (int32_t)((t0 + t) * 128), bar);
       }
     };
-    for (; loaded < kTcStages - 1 && loaded < mine; ++loaded) load(loaded);
+    for (; loaded < kTcStages && loaded < mine; ++loaded) load(loaded);
     for (int64_t i = 0; i < mine && ok; ++i) {
       const int s = (int)(i % kTcStages), a = (int)(i % kTcAcc);
       ok = __all_sync(kFull, tc_wait(full0 + 8u * s, (uint32_t)((i / kTcStages) & 1), &stop));
@@ -243,14 +246,13 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
       }
       __syncwarp();
       issued = i + 1;
-      // refill the stage batch i - 1 used, once its products are done
-      if (loaded < mine && i >= 1) {
-        const int64_t k = i - 1;
+      // refill the stage of batch i - kTcRefillLag (its products finished long ago) with batch
+      // i - kTcRefillLag + kTcStages: the copies stay kTcStages - kTcRefillLag batches ahead
+      const int64_t k = i - kTcRefillLag;
+      if (k >= 0 && loaded < mine) {
         ok = __all_sync(kFull, tc_wait(sfree0 + 8u * (uint32_t)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), &stop));
         if (!ok) break;
         load(loaded++);
-      } else if (loaded < mine) {
-        load(loaded++);                        // i == 0: the last free stage
       }
     }
     if (!ok) {
@@ -262,7 +264,7 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
       for (int64_t k = issued; k < loaded; ++k)
         if (!mbar_wait(full0 + 8u * (uint32_t)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), kSpinLimit) && lane == 0)
           atomicOr(&g_fp4q_fault, kFaultDrainWait);
-      for (int64_t k = issued > kTcStages ? issued - kTcStages : 0; k < issued; ++k)
+      for (int64_t k = issued > kTcStages ? issued - kTcStages : 0; k < issued; ++k)   // no later use of those stages
         if (!mbar_wait(sfree0 + 8u * (uint32_t)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), kSpinLimit) && lane == 0)
           atomicOr(&g_fp4q_fault, kFaultDrainWait);
     }
