@@ -1764,13 +1764,14 @@ EncodeTiled encode_fn() {
 
 // 2-D view of a contiguous buffer as 128-byte lines, one 8-block tile per box, 128-byte
 // swizzle (bfloat16: 64 elements per line, 32 lines per tile; float32: 32 and 64).
-bool line_map(CUtensorMap* m, const void* ptr, int64_t n, bool f32) {
+bool line_map(CUtensorMap* m, const void* ptr, int64_t n, bool f32, int box_lines = 0) {
   EncodeTiled enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t per_line = f32 ? 32 : 64;
   const cuuint64_t dims[2] = {per_line, (cuuint64_t)(n / (int64_t)per_line)};
   const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {(cuuint32_t)per_line, (cuuint32_t)(f32 ? kTileLinesF32 : kTileLinesBF16)};
+  const cuuint32_t box[2] = {(cuuint32_t)per_line,
+                             (cuuint32_t)(box_lines ? box_lines : (f32 ? kTileLinesF32 : kTileLinesBF16))};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1793,21 +1794,6 @@ bool rows_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64
   return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// The tensor-core compress reads a contiguous BF16 tensor as rows of 16 elements (32 bytes,
-// one group), 128 rows (one 8-block tile) per box, with the 32-byte swizzle its MMA operand
-// layout expects.
-bool group_rows_map(CUtensorMap* m, const void* ptr, int64_t n) {
-  EncodeTiled enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {16, (cuuint64_t)(n / 16)};
-  const cuuint64_t strides[1] = {32};
-  const cuuint32_t box[2] = {16, 128};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1885,8 +1871,8 @@ fp4q_status launch_compress_tc(const void* x, int64_t n, const Payload& P, cudaS
   if (nfull > 0) {
     const int64_t nb = nfull / FP4Q_BLOCK, tiles = (nb + kTileBlocks - 1) / kTileBlocks;
     const int64_t batches = (tiles + kTcTiles - 1) / kTcTiles;
-    CUtensorMap xm;
-    if (!group_rows_map(&xm, x, nfull)) return FP4Q_ERR_CUDA;
+    CUtensorMap xm;   // 128-byte lines (quarter-blocks), one box of 128 lines (32 blocks) per batch
+    if (!line_map(&xm, x, nfull, false, 4 * kTcTiles * kTileBlocks)) return FP4Q_ERR_CUDA;
     auto k = compress_tc_kernel<G>;
     Launch L;
     // plan() sizes the grid as (units / warps) CTAs: one unit per warp and batch gives one CTA

@@ -2,25 +2,28 @@
 // Included by fp4q.cu inside its anonymous namespace, after the shared helpers.
 //
 // The method: "FP4Quant" (shd-paper.top), technical framework: a hybrid two-level FWHT in a
-// GPU-aware pipeline. H256 = H16 (x) H16, so y = (1/16) H16 X H16 for a block viewed as the
-// 16 x 16 matrix X[g][p] (g = group, p = position in the group). This encoder evaluates the
-// level that mixes groups as a +-1 matrix product on the 5th-generation tensor cores and the
-// level inside a group in registers:
-//   D = Hbd * Xt    (tcgen05.mma kind::f16, BF16 operands, FP32 accumulation in TMEM)
-// where Xt is the BF16 input of 4 consecutive 8-block tiles exactly as the TMA loads it
-// (rows k = (block, g) of 16 positions, 32-byte swizzle: a K x N = 128 x 64 MN-major operand),
-// and Hbd is the 128 x 128 block-diagonal matrix of eight H16 blocks, applied as eight
-// K = 16 slices (slice j holds H16 in rows 16j .. 16j+15; every slice is a window of one
-// 240-row buffer that has H16 in rows 112 .. 127 and zeros elsewhere). Each TMEM lane then
-// holds one row (block, g') of the group-mixed values for 16 positions; a thread loads it
-// with tcgen05.ld, applies H16 along the positions with FP32 butterflies (one quantisation
-// group per thread) and quantises it as the contract's Scales / Codes / Packing steps do.
+// GPU-aware pipeline. A block of 256 elements is x[g][p] (g = group of 16, p = position in
+// the group) and H256 = H16 (x) H16; with H16 = H4 (x) H4 the group index splits further into
+// g = 4 gh + gl. This encoder evaluates the part of the transform that mixes the four
+// quarter-blocks (gh, two butterfly stages) as a +-1 matrix product on the 5th-generation
+// tensor cores and the remaining six stages in registers:
+//   D = Hq * Xq    (tcgen05.mma kind::f16, BF16 operands, FP32 accumulation in TMEM)
+// where Xq is the BF16 input of 32 consecutive blocks exactly as the TMA loads it (128-byte
+// lines of 64 elements, each a quarter-block (block, gh); 128-byte swizzle: a K x N = 128 x 64
+// MN-major operand), and Hq is the block-diagonal 128 x 128 matrix of 32 H4 blocks, applied as
+// eight K = 16 slices (slice j holds four H4 blocks in rows 16j .. 16j+15; every slice is a
+// window of one 240-row buffer that has them in rows 112 .. 127 and zeros elsewhere). TMEM
+// lane (block, gh') then holds the 64 values (gl, p) of that quarter-block after the mixing;
+// its thread loads them with tcgen05.ld, applies H4 across gl and H16 along p with FP32
+// butterflies and holds the four groups 4 gh' + gl' of the block: the row layout of the
+// tiled kernels (four lanes per block, four groups per lane), so the same quantisation and
+// store run on it.
 //
-// The products are exact (BF16 times +-1) but the tensor core accumulates the 16 terms of
-// each sum in its own order, and the levels run in the other order than the contract's
-// butterfly sequence, so y matches the contract only to FP32 rounding: scales and codes can
-// differ where the contract's value sits on a rounding boundary. The payload format is the
-// contract's, and every decoder reads it as an fwht = 1 payload.
+// The products are exact (BF16 times +-1) but the tensor core accumulates each 4-term sum in
+// its own order and the stages run in another order than the contract's butterfly sequence,
+// so y matches the contract only to FP32 rounding: scales and codes can differ where the
+// contract's value sits on a rounding boundary. The payload format is the contract's, and
+// every decoder reads it as an fwht = 1 payload.
 //
 // Pipeline (warp-specialised, one persistent CTA per SM): a producer warp keeps
 // kTcStages - kTcRefillLag batches of 4 tiles ahead in flight by TMA and issues the eight MMAs of each
@@ -33,14 +36,14 @@
 // flag, the producer waits (bounded) for the copies and products it issued, and the CTA frees
 // its TMEM.
 
-constexpr int kTcTiles = 4;                          // 8-block tiles per batch (MMA N = 64)
+constexpr int kTcTiles = 4;                          // 8-block tiles per batch (32 blocks, 128 quarter-block rows)
 constexpr int kTcGroups = 4;                         // consumer warpgroups
 constexpr int kTcAcc = 2 * kTcGroups;                // TMEM accumulators (two per warpgroup)
 constexpr int kTcStages = 8;                         // input batches buffered per CTA
 constexpr int kTcRefillLag = 2;                      // a stage is refilled this many batches after its MMAs
 constexpr int kTcBatchBytes = kTcTiles * 4096;       // BF16 input of one batch
 constexpr int kTcZBytes = 8192;                      // A operand buffer (240 rows used)
-constexpr int kTcAccCols = 16 * kTcTiles;            // TMEM columns of one FP32 accumulator
+constexpr int kTcAccCols = 64;                       // TMEM columns of one FP32 accumulator (MMA N)
 constexpr uint32_t kTcTmemCols = kTcAcc * kTcAccCols;  // 512: the whole TMEM of the SM
 constexpr int kTcThreads = 32 * (4 * kTcGroups + 1);   // consumers + one producer warp
 constexpr int kTcSmemBytes = 1024 + kTcZBytes + kTcStages * kTcBatchBytes;
@@ -58,9 +61,10 @@ constexpr uint32_t kTcIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                               ((uint32_t)(kTcAccCols >> 3) << 17) | ((128u >> 4) << 24);
 // Operand layouts (checked on the hardware against a CPU product): A K-major without swizzle,
 // core matrices of 8 rows x 16 bytes, K-group stride 128 bytes (LBO), row-group stride 256
-// (SBO); B MN-major with the 32-byte swizzle the TMA writes, 16-column group stride 4096 bytes
-// (one tile; LBO), 8-row group stride 256 bytes (SBO).
-constexpr uint32_t kTcALbo = 128, kTcASbo = 256, kTcBLbo = 4096, kTcBSbo = 256;
+// (SBO); B MN-major with the 128-byte swizzle the TMA writes, rows of 64 elements, 8-row group
+// stride 1024 bytes (SBO; with N = 64 the leading offset is not used).
+constexpr uint32_t kTcALbo = 128, kTcASbo = 256, kTcBLbo = 16, kTcBSbo = 1024;
+constexpr uint32_t kUmmaSwizzle128B = 2;
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -84,67 +88,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t r[16]) {
                : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Quantised row: the 16 codes of one group row, its group-scale code and the block scale.
-struct RowQ {
-  uint32_t w0, w1, sg;
-  float sb;
-};
-
-// Dual-scale quantisation of one 16-element row per thread; the 16 lanes of a half-warp hold
-// the 16 rows of one block. v is the unnormalised transform z = 16 y (the scales fold the
-// 1/16 as the tiled kernels do).
-template <int G>
-__device__ __forceinline__ void quantize_row(const float2 v[8], RowQ& o) {
-  float a[16];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    a[2 * j] = fabsf(v[j].x);
-    a[2 * j + 1] = fabsf(v[j].y);
-  }
-  const float m0 = max3(a[0], a[1], a[2]), m1 = max3(a[3], a[4], a[5]), m2 = max3(a[6], a[7], a[8]);
-  const float m3 = max3(a[9], a[10], a[11]), m4 = max3(a[12], a[13], a[14]);
-  float am = max3(max3(m0, m1, m2), fmaxf(m3, m4), a[15]);
-  float A = am;
-#pragma unroll
-  for (int k = 1; k < 16; k <<= 1) A = fmaxf(A, __shfl_xor_sync(kFull, A, k));
-  if (G == 32) am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));
-  A = __fmul_rn(A, 0.0625f);
-  am = __fmul_rn(am, 0.0625f);
-  const bool zero = !(A >= kZeroLimit);
-  const float sb = zero ? 0.0f : fp4q_math::div_rn_2688(A);
-  const float tb = zero ? 1.0f : __fmul_rn(sb, 6.0f);
-  const fp4q_math::Divider by_tb(tb);
-  uint32_t c = e4m3x2(by_tb.div(am), 0.0f) & 0xffu;
-  if (zero) c = 0u;
-  const float S = __fmul_rn(e4m3x2_to_f2(c).x, sb);
-  float inv = S > 0.0f ? fp4q_math::rcp_rn(S) : 0.0f;
-  inv = __fmul_rn(inv, 0.0625f);
-  const float2 iv = make_float2(inv, inv);
-  uint32_t w0 = e2m1_pack8(mul2(v[0], iv), mul2(v[1], iv), mul2(v[2], iv), mul2(v[3], iv));
-  uint32_t w1 = e2m1_pack8(mul2(v[4], iv), mul2(v[5], iv), mul2(v[6], iv), mul2(v[7], iv));
-  if (zero) w0 = w1 = 0u;
-  o.w0 = w0;
-  o.w1 = w1;
-  o.sg = c;
-  o.sb = sb;
-}
-
-// Store one row (group row g of block gb): 8 bytes of codes, its group-scale byte (G = 16;
-// for G = 32 the even row of the pair), the block scale from row 0.
-template <int G>
-__device__ __forceinline__ void store_row(const Payload& P, int64_t gb, int g, const RowQ& q) {
-  *reinterpret_cast<uint2*>(P.codes + gb * 128 + g * 8) = make_uint2(q.w0, q.w1);
-  if (G == 16) {
-    P.gsc[gb * 16 + g] = (uint8_t)q.sg;
-  } else if (!(g & 1)) {
-    P.gsc[gb * 8 + (g >> 1)] = (uint8_t)q.sg;
-  }
-  if (g == 0) {
-    P.bsc[gb] = q.sb;
-    if (G == 32 && (P.nb & 1) && gb == P.nb - 1) *reinterpret_cast<uint2*>(P.gsc + 8 * P.nb) = make_uint2(0u, 0u);
-  }
-}
 
 // One poll loop of the pipeline: bounded, and it also gives up when another thread of the CTA
 // has already given up (stop flag in shared memory).
@@ -172,17 +115,19 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
   const uint32_t stage0 = zbuf + kTcZBytes;
   const uint32_t full0 = smem_addr(&bars[0]), sfree0 = full0 + 8u * kTcStages;
   const uint32_t afull0 = sfree0 + 8u * kTcStages, afree0 = afull0 + 8u * kTcAcc;
-  const int64_t tiles = (nb + kTileBlocks - 1) / kTileBlocks;
 
   // A operand: row r, column k at (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2;
-  // rows 112 .. 127 hold H16 (entry (i, k) = (-1)^popcount(i & k), exact in BF16), the rest 0.
+  // rows 112 .. 127 hold four H4 blocks on the diagonal (entry (i, k) = (-1)^popcount(i & k)
+  // when i / 4 == k / 4, exact in BF16), the rest 0.
   for (int u = tid; u < kTcZBytes / 16; u += kTcThreads) {
     const int r = 8 * (u >> 4) + (u & 7), k0 = 8 * ((u >> 3) & 1);
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     if (r >= 112 && r < 128) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const uint32_t h = (__popc((uint32_t)((r - 112) & (k0 + e))) & 1) ? 0xBF80u : 0x3F80u;
+        const int i = r - 112, k = k0 + e;
+        if ((i >> 2) != (k >> 2)) continue;
+        const uint32_t h = (__popc((uint32_t)(i & k & 3)) & 1) ? 0xBF80u : 0x3F80u;
         w[e >> 1] |= h << (16 * (e & 1));
       }
     }
@@ -220,12 +165,11 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
     int64_t loaded = 0, issued = 0;
     bool ok = true;
     auto load = [&](int64_t i) {               // lane 0: TMA of batch i into stage i % kTcStages
-      const int64_t t0 = (first + i * step) * kTcTiles;
-      const int nt = (int)(tiles - t0 < kTcTiles ? tiles - t0 : kTcTiles);
       const uint32_t st = stage0 + (uint32_t)((i % kTcStages) * kTcBatchBytes), bar = full0 + 8u * (uint32_t)(i % kTcStages);
       if (lane == 0) {
-        mbar_expect_tx(bar, (uint32_t)nt * 4096u);
-        for (int t = 0; t < nt; ++t) tma_load_2d(st + 4096u * (uint32_t)t, &xmap, 0, (int32_t)((t0 + t) * 128), bar);
+        // one box of 128 lines = 32 blocks (lines past the tensor's end read as zeros)
+        mbar_expect_tx(bar, (uint32_t)kTcBatchBytes);
+        tma_load_2d(st, &xmap, 0, (int32_t)((first + i * step) * 128), bar);
       }
     };
     for (; loaded < kTcStages && loaded < mine; ++loaded) load(loaded);
@@ -240,7 +184,7 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           umma_bf16(d, umma_desc(zbuf + (uint32_t)(14 - 2 * j) * 256u, kTcALbo, kTcASbo, 0),
-                    umma_desc(st + 512u * (uint32_t)j, kTcBLbo, kTcBSbo, kUmmaSwizzle32B), j > 0);
+                    umma_desc(st + 2048u * (uint32_t)j, kTcBLbo, kTcBSbo, kUmmaSwizzle128B), j > 0);
         umma_commit(afull0 + 8u * a);
         umma_commit(sfree0 + 8u * s);
       }
@@ -271,7 +215,7 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
   } else {
     // ---------------------------------------------------------------- consumer warpgroups
     const int grp = warp >> 2, wq = warp & 3;   // warpgroup, and its quarter of the TMEM lanes
-    const int row = wq * 32 + lane, g = lane & 15;
+    const int l4 = lane & 3;                    // gh' of the lane's quarter-block (four lanes per block)
     for (int64_t i = grp; i < mine; i += kTcGroups) {
       const int a = (int)(i % kTcAcc);
       if (!__all_sync(kFull, tc_wait(afull0 + 8u * a, (uint32_t)((i / kTcAcc) & 1), &stop))) {
@@ -283,32 +227,29 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
       }
       tc_fence_after();
       const uint32_t acc = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * kTcAccCols);
-      uint32_t r[kTcTiles][16];
+      uint32_t r[4][16];
 #pragma unroll
-      for (int t = 0; t < kTcTiles; ++t) tmem_ld16(acc + 16u * (uint32_t)t, r[t]);
+      for (int k = 0; k < 4; ++k) tmem_ld16(acc + 16u * (uint32_t)k, r[k]);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(afree0 + 8u * a) : "memory");
-      const int64_t t0 = (first + i * step) * kTcTiles;
+      Rows v;                                   // v[gl][j]: positions 2j, 2j + 1 of group gl
 #pragma unroll
-      for (int t = 0; t < kTcTiles; ++t) {
-        float2 v[8];
+      for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = make_float2(__uint_as_float(r[t][2 * j]), __uint_as_float(r[t][2 * j + 1]));
-        // the level inside a group: H16 along the 16 positions (strides 1, 2, 4, 8)
+        for (int j = 0; j < 8; ++j) v[k][j] = make_float2(__uint_as_float(r[k][2 * j]), __uint_as_float(r[k][2 * j + 1]));
+      rows_bfly(v, 1);                          // H4 across gl
+      rows_bfly(v, 2);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) bfly_in(v[j]);
+      for (int k = 0; k < 4; ++k)               // H16 along p (strides 1, 2, 4, 8)
 #pragma unroll
-        for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (!(j & h)) bfly2(v[j], v[j + h]);
-        RowQ q;
-        quantize_row<G>(v, q);
-        const int64_t gb = (t0 + t) * kTileBlocks + (row >> 4);
-        if (t0 + t < tiles && gb < nb) store_row<G>(P, gb, g, q);
-      }
+        for (int j = 0; j < 8; ++j) bfly_in(v[k][j]);
+      level1_fwd_from2(v);
+      Quant q;
+      quantize<G, false, true>(v, q);
+      const int64_t gb = (first + i * step) * (kTcTiles * kTileBlocks) + 8 * wq + (lane >> 2);
+      if (gb < nb) store_block<G, false, false>(P, gb, l4, q);
     }
   }
   tc_fence_before();
