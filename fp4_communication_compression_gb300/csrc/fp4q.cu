@@ -1869,10 +1869,9 @@ template <int G>
 fp4q_status launch_compress_tc(const void* x, int64_t n, const Payload& P, cudaStream_t s) {
   const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
   if (nfull > 0) {
-    const int64_t nb = nfull / FP4Q_BLOCK, tiles = (nb + kTileBlocks - 1) / kTileBlocks;
-    const int64_t batches = (tiles + kTcTiles - 1) / kTcTiles;
-    CUtensorMap xm;   // 128-byte lines (quarter-blocks), one box of 128 lines (32 blocks) per batch
-    if (!line_map(&xm, x, nfull, false, 4 * kTcTiles * kTileBlocks)) return FP4Q_ERR_CUDA;
+    const int64_t nb = nfull / FP4Q_BLOCK, batches = (nb + kTcBatchBlocks - 1) / kTcBatchBlocks;
+    CUtensorMap xm;   // 128-byte lines (quarter-blocks), boxes of 256 lines (64 blocks), two per batch
+    if (!line_map(&xm, x, nfull, false, 2 * kTcBatchBlocks)) return FP4Q_ERR_CUDA;
     auto k = compress_tc_kernel<G>;
     Launch L;
     // plan() sizes the grid as (units / warps) CTAs: one unit per warp and batch gives one CTA

@@ -8,9 +8,10 @@
 // quarter-blocks (gh, two butterfly stages) as a +-1 matrix product on the 5th-generation
 // tensor cores and the remaining six stages in registers:
 //   D = Hq * Xq    (tcgen05.mma kind::f16, BF16 operands, FP32 accumulation in TMEM)
-// where Xq is the BF16 input of 32 consecutive blocks exactly as the TMA loads it (128-byte
-// lines of 64 elements, each a quarter-block (block, gh); 128-byte swizzle: a K x N = 128 x 64
-// MN-major operand), and Hq is the block-diagonal 128 x 128 matrix of 32 H4 blocks, applied as
+// where Xq is the BF16 input of 4 x 32 consecutive blocks exactly as the TMA loads it (128-byte
+// lines of 64 elements, each a quarter-block (block, gh); 128-byte swizzle): the four 32-block
+// sub-batches side by side form a K x N = 128 x 256 MN-major operand whose K index (block within
+// the sub-batch, gh) they share. Hq is the block-diagonal 128 x 128 matrix of 32 H4 blocks, applied as
 // eight K = 16 slices (slice j holds four H4 blocks in rows 16j .. 16j+15; every slice is a
 // window of one 240-row buffer that has them in rows 112 .. 127 and zeros elsewhere). TMEM
 // lane (block, gh') then holds the 64 values (gl, p) of that quarter-block after the mixing;
@@ -25,26 +26,30 @@
 // contract's value sits on a rounding boundary. The payload format is the contract's, and
 // every decoder reads it as an fwht = 1 payload.
 //
-// Pipeline (warp-specialised, one persistent CTA per SM): a producer warp keeps
-// kTcStages - kTcRefillLag batches of 4 tiles ahead in flight by TMA and issues the eight MMAs of each
-// batch as soon as its input has landed and its TMEM accumulator is free; kTcGroups consumer
-// warpgroups take the batches in turn, each with its own pair of accumulators: a consumer
-// copies an accumulator to registers (one tcgen05.ld of 64 columns), frees it at once, then
-// applies the in-group level and quantises while the tensor cores fill the next one. MMA
-// completion is signalled with tcgen05.commit to mbarriers (accumulator full, input stage
-// free). Every wait is bounded; a wait that gives up sets the fault word and a CTA-wide stop
-// flag, the producer waits (bounded) for the copies and products it issued, and the CTA frees
-// its TMEM.
+// Pipeline (warp-specialised, one persistent CTA per SM). A batch is 128 consecutive blocks
+// (four sub-batches of 32, side by side in the MMA's N dimension: N = 256, so each MMA
+// instruction covers 4 x 32 blocks; at N = 64 the producer spent ~80 cycles issuing each
+// MMA and paced the whole pipeline). A producer warp keeps kTcStages - kTcRefillLag batches
+// in flight by TMA and issues the eight MMAs of each batch into one of two 256-column TMEM
+// accumulators as soon as its input has landed and the accumulator is free; each of the
+// kTcGroups consumer warpgroups takes one sub-batch (64 columns) of every batch, copies it
+// to registers (one tcgen05.ld of 64 columns), frees it, then applies the in-register stages
+// and quantises while the tensor cores fill the other accumulator. MMA completion is signalled
+// with tcgen05.commit to mbarriers (accumulator full, input stage free). Every wait is
+// bounded; a wait that gives up sets the fault word and a CTA-wide stop flag, the producer
+// waits (bounded) for the copies and products it issued, and the CTA frees its TMEM.
 
-constexpr int kTcTiles = 4;                          // 8-block tiles per batch (32 blocks, 128 quarter-block rows)
-constexpr int kTcGroups = 4;                         // consumer warpgroups
-constexpr int kTcAcc = 2 * kTcGroups;                // TMEM accumulators (two per warpgroup)
-constexpr int kTcStages = 8;                         // input batches buffered per CTA
-constexpr int kTcRefillLag = 2;                      // a stage is refilled this many batches after its MMAs
-constexpr int kTcBatchBytes = kTcTiles * 4096;       // BF16 input of one batch
-constexpr int kTcZBytes = 8192;                      // A operand buffer (240 rows used)
-constexpr int kTcAccCols = 64;                       // TMEM columns of one FP32 accumulator (MMA N)
+constexpr int kTcGroups = 4;                         // consumer warpgroups = sub-batches per batch
+constexpr int kTcSubBlocks = 32;                     // blocks per sub-batch (128 quarter-block rows = MMA M, K)
+constexpr int kTcBatchBlocks = kTcGroups * kTcSubBlocks;
+constexpr int kTcSubBytes = kTcSubBlocks * 512;      // BF16 input of one sub-batch (16 KiB)
+constexpr int kTcBatchBytes = kTcGroups * kTcSubBytes;
+constexpr int kTcAcc = 2;                            // TMEM accumulators
+constexpr int kTcAccCols = 64 * kTcGroups;           // MMA N: 256 FP32 columns per accumulator
 constexpr uint32_t kTcTmemCols = kTcAcc * kTcAccCols;  // 512: the whole TMEM of the SM
+constexpr int kTcStages = 3;                         // input batches buffered per CTA
+constexpr int kTcRefillLag = 1;                      // a stage is refilled this many batches after its MMAs
+constexpr int kTcZBytes = 8192;                      // A operand buffer (240 rows used)
 constexpr int kTcThreads = 32 * (4 * kTcGroups + 1);   // consumers + one producer warp
 constexpr int kTcSmemBytes = 1024 + kTcZBytes + kTcStages * kTcBatchBytes;
 
@@ -62,8 +67,8 @@ constexpr uint32_t kTcIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
 // Operand layouts (checked on the hardware against a CPU product): A K-major without swizzle,
 // core matrices of 8 rows x 16 bytes, K-group stride 128 bytes (LBO), row-group stride 256
 // (SBO); B MN-major with the 128-byte swizzle the TMA writes, rows of 64 elements, 8-row group
-// stride 1024 bytes (SBO; with N = 64 the leading offset is not used).
-constexpr uint32_t kTcALbo = 128, kTcASbo = 256, kTcBLbo = 16, kTcBSbo = 1024;
+// stride 1024 bytes (SBO), 64-column group stride one sub-batch (LBO).
+constexpr uint32_t kTcALbo = 128, kTcASbo = 256, kTcBLbo = kTcSubBytes, kTcBSbo = 1024;
 constexpr uint32_t kUmmaSwizzle128B = 2;
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
@@ -91,10 +96,18 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 
 // One poll loop of the pipeline: bounded, and it also gives up when another thread of the CTA
 // has already given up (stop flag in shared memory).
+// BACKOFF: sleep between polls (consumer warps, which wait for most of a batch: spinning, they
+// would take issue slots from the producer warp that shares their sub-partition).
+template <bool BACKOFF>
 __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, const volatile uint32_t* stop) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
+  uint32_t sleep_ns = 32;
   for (uint32_t k = 1; k < kSpinLimit; ++k) {
+    if (BACKOFF) {
+      __nanosleep(sleep_ns);
+      if (sleep_ns < 256) sleep_ns <<= 1;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     if ((k & 63u) == 0u && (*stop || global_ns() - t0 > kWaitLimitNs)) return false;
   }
@@ -140,7 +153,7 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
     }
     for (int a = 0; a < kTcAcc; ++a) {
       mbar_init(afull0 + 8u * a, 1);
-      mbar_init(afree0 + 8u * a, 4);
+      mbar_init(afree0 + 8u * a, 4 * kTcGroups);
     }
     stop = 0u;
     fence_barrier_init();
@@ -167,24 +180,31 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
     auto load = [&](int64_t i) {               // lane 0: TMA of batch i into stage i % kTcStages
       const uint32_t st = stage0 + (uint32_t)((i % kTcStages) * kTcBatchBytes), bar = full0 + 8u * (uint32_t)(i % kTcStages);
       if (lane == 0) {
-        // one box of 128 lines = 32 blocks (lines past the tensor's end read as zeros)
+        // two boxes of 256 lines = 128 blocks (lines past the tensor's end read as zeros)
+        const int32_t line0 = (int32_t)((first + i * step) * (4 * kTcBatchBlocks));
         mbar_expect_tx(bar, (uint32_t)kTcBatchBytes);
-        tma_load_2d(st, &xmap, 0, (int32_t)((first + i * step) * 128), bar);
+        tma_load_2d(st, &xmap, 0, line0, bar);
+        tma_load_2d(st + kTcBatchBytes / 2, &xmap, 0, line0 + 2 * kTcBatchBlocks, bar);
       }
     };
+    // descriptors: the A slices are fixed; a B slice differs from the first stage's first slice
+    // only in the start-address field (address >> 4, which stays below 2^14 inside shared memory)
+    uint64_t adesc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adesc[j] = umma_desc(zbuf + (uint32_t)(14 - 2 * j) * 256u, kTcALbo, kTcASbo, 0);
+    const uint64_t bdesc0 = umma_desc(stage0, kTcBLbo, kTcBSbo, kUmmaSwizzle128B);
     for (; loaded < kTcStages && loaded < mine; ++loaded) load(loaded);
     for (int64_t i = 0; i < mine && ok; ++i) {
       const int s = (int)(i % kTcStages), a = (int)(i % kTcAcc);
-      ok = __all_sync(kFull, tc_wait(full0 + 8u * s, (uint32_t)((i / kTcStages) & 1), &stop));
-      if (ok && i >= kTcAcc) ok = __all_sync(kFull, tc_wait(afree0 + 8u * a, (uint32_t)(((i / kTcAcc) - 1) & 1), &stop));
+      ok = __all_sync(kFull, tc_wait<false>(full0 + 8u * s, (uint32_t)((i / kTcStages) & 1), &stop));
+      if (ok && i >= kTcAcc) ok = __all_sync(kFull, tc_wait<false>(afree0 + 8u * a, (uint32_t)(((i / kTcAcc) - 1) & 1), &stop));
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t st = stage0 + (uint32_t)(s * kTcBatchBytes), d = tmem + (uint32_t)(a * kTcAccCols);
+        const uint32_t d = tmem + (uint32_t)(a * kTcAccCols);
+        const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)(s * kTcBatchBytes) >> 4);   // + 128 per K-slice (16 rows)
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          umma_bf16(d, umma_desc(zbuf + (uint32_t)(14 - 2 * j) * 256u, kTcALbo, kTcASbo, 0),
-                    umma_desc(st + 2048u * (uint32_t)j, kTcBLbo, kTcBSbo, kUmmaSwizzle128B), j > 0);
+        for (int j = 0; j < 8; ++j) umma_bf16(d, adesc[j], bd + (uint64_t)(128u * (uint32_t)j), j > 0);
         umma_commit(afull0 + 8u * a);
         umma_commit(sfree0 + 8u * s);
       }
@@ -194,7 +214,7 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
       // i - kTcRefillLag + kTcStages: the copies stay kTcStages - kTcRefillLag batches ahead
       const int64_t k = i - kTcRefillLag;
       if (k >= 0 && loaded < mine) {
-        ok = __all_sync(kFull, tc_wait(sfree0 + 8u * (uint32_t)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), &stop));
+        ok = __all_sync(kFull, tc_wait<false>(sfree0 + 8u * (uint32_t)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), &stop));
         if (!ok) break;
         load(loaded++);
       }
@@ -214,11 +234,11 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
     }
   } else {
     // ---------------------------------------------------------------- consumer warpgroups
-    const int grp = warp >> 2, wq = warp & 3;   // warpgroup, and its quarter of the TMEM lanes
+    const int grp = warp >> 2, wq = warp & 3;   // warpgroup (= sub-batch), its quarter of the TMEM lanes
     const int l4 = lane & 3;                    // gh' of the lane's quarter-block (four lanes per block)
-    for (int64_t i = grp; i < mine; i += kTcGroups) {
+    for (int64_t i = 0; i < mine; ++i) {
       const int a = (int)(i % kTcAcc);
-      if (!__all_sync(kFull, tc_wait(afull0 + 8u * a, (uint32_t)((i / kTcAcc) & 1), &stop))) {
+      if (!__all_sync(kFull, tc_wait<true>(afull0 + 8u * a, (uint32_t)((i / kTcAcc) & 1), &stop))) {
         if (lane == 0) {
           stop = 1u;
           atomicOr(&g_fp4q_fault, kFaultLoadWait);
@@ -226,7 +246,7 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
         break;
       }
       tc_fence_after();
-      const uint32_t acc = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * kTcAccCols);
+      const uint32_t acc = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * kTcAccCols + 64 * grp);
       uint32_t r[4][16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) tmem_ld16(acc + 16u * (uint32_t)k, r[k]);
@@ -248,7 +268,7 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
       level1_fwd_from2(v);
       Quant q;
       quantize<G, false, true>(v, q);
-      const int64_t gb = (first + i * step) * (kTcTiles * kTileBlocks) + 8 * wq + (lane >> 2);
+      const int64_t gb = (first + i * step) * kTcBatchBlocks + kTcSubBlocks * grp + 8 * wq + (lane >> 2);
       if (gb < nb) store_block<G, false, false>(P, gb, l4, q);
     }
   }
