@@ -66,11 +66,12 @@
  *            the transform domain (no inverse FWHT), then Scales/Codes/Packing on z with
  *            no forward FWHT. [P3 "Read it as": the AllReduce of tensor parallelism]
  *   Tensor-core encoder (fwht = 2; relaxed, opt-in) [P1 "hybrid two-level FWHT pipeline",
- *            "GPU-aware execution optimization"]: the same y = H256 x / 16, with the level
- *            that mixes the 16 groups of a block computed first, as a +-1 BF16 matrix product
- *            on the tensor cores (exact products, FP32 accumulation in the hardware's order),
- *            then the level inside each group as FP32 butterflies. y agrees with the FWHT
- *            step above to FP32 rounding only (about 1e-6 of the block maximum), so a scale
+ *            "GPU-aware execution optimization"]: the same y = H256 x / 16, with the two
+ *            butterfly stages that mix the four quarter-blocks of a block (strides 64 and 128)
+ *            computed first, as a +-1 BF16 matrix product on the tensor cores (exact products,
+ *            FP32 accumulation in the hardware's order), then the other six stages as FP32
+ *            butterflies. y agrees with the FWHT step above to FP32 rounding only (about 1e-6
+ *            of the block maximum), so a scale
  *            or a code whose contract value lies on a rounding boundary can differ; the
  *            payload format is unchanged and decodes as an fwht = 1 payload. Contiguous
  *            BF16 input and dual scales only (fp4q_compress, fp4q_compress_segments); the
