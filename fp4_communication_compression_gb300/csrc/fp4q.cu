@@ -351,10 +351,17 @@ struct Quant {
   float sb;              // block scale
 };
 
-// Dual-scale quantisation of the lane's rows (rows in layout A if !LB, layout B if LB).
+// Dual scales of the lane's rows (rows in layout A if !LB, layout B if LB): the group-scale
+// codes, the decode scale S and the quantisation multiplier inv of each row, the block scale.
 // FOLD: the values are the unnormalised transform z = 16 y (see the file header).
+struct DualScales {
+  float S[4], inv[4], sb;
+  uint32_t sg;
+  bool zero;
+};
+
 template <int G, bool LB, bool FOLD>
-__device__ __forceinline__ void quantize(const Rows v, Quant& o) {
+__device__ __forceinline__ void dual_scales(const Rows v, DualScales& o) {
   float am[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -400,18 +407,69 @@ __device__ __forceinline__ void quantize(const Rows v, Quant& o) {
   const float sgv[4] = {s01.x, s01.y, s23.x, s23.y};
   o.sg = c01 | (c23 << 16);
   o.sb = sb;
+  o.zero = zero;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const float S = __fmul_rn(sgv[k], sb);
     o.S[k] = S;
     float inv = S > 0.0f ? fp4q_math::rcp_rn(S) : 0.0f;
     if (FOLD) inv = __fmul_rn(inv, 0.0625f);
-    const float2 iv = make_float2(inv, inv);
+    o.inv[k] = inv;
+  }
+}
+
+// Dual-scale quantisation of the lane's rows: codes, scales.
+template <int G, bool LB, bool FOLD>
+__device__ __forceinline__ void quantize(const Rows v, Quant& o) {
+  DualScales sc;
+  dual_scales<G, LB, FOLD>(v, sc);
+  o.sg = sc.sg;
+  o.sb = sc.sb;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    o.S[k] = sc.S[k];
+    const float2 iv = make_float2(sc.inv[k], sc.inv[k]);
     uint32_t w0 = e2m1_pack8(mul2(v[k][0], iv), mul2(v[k][1], iv), mul2(v[k][2], iv), mul2(v[k][3], iv));
     uint32_t w1 = e2m1_pack8(mul2(v[k][4], iv), mul2(v[k][5], iv), mul2(v[k][6], iv), mul2(v[k][7], iv));
-    if (zero) w0 = w1 = 0u;
+    if (sc.zero) w0 = w1 = 0u;
     o.code[k][0] = w0;
     o.code[k][1] = w1;
+  }
+}
+
+// One value pair -> its E2M1 codes -> their grid values (exact): the code byte never leaves
+// the conversion, for the fused roundtrip, which writes no payload.
+__device__ __forceinline__ float2 e2m1_round_pair(float2 q) {
+  uint32_t h;
+  asm("{.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;}"
+      : "=r"(h) : "f"(q.x), "f"(q.y));
+  const __half2 t = *reinterpret_cast<const __half2*>(&h);
+  return make_float2(__low2float(t), __high2float(t));
+}
+
+// quantize followed by dequantize, for the fused roundtrip: v (the transform values) becomes
+// x~ * dscale (dscale = 1/16 folds the inverse transform's normalisation into the decode
+// scale, as scale_by_16th does). Bit-identical to the two steps: the same conversions in the
+// same order, without packing the codes into words and unpacking them again; an all-zero block
+// decodes to +0, as its zeroed codes do.
+template <int G, bool LB, bool FOLD>
+__device__ __forceinline__ void quantize_decode(Rows v, float dscale, float nz) {
+  DualScales sc;
+  dual_scales<G, LB, FOLD>(v, sc);
+  const float2 z2 = make_float2(nz, nz);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 iv = make_float2(sc.inv[k], sc.inv[k]);
+    const float Sd = __fmul_rn(sc.S[k], dscale);
+    const float2 s = make_float2(Sd, Sd);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[k][j] = fma2(e2m1_round_pair(mul2(v[k][j], iv)), s, z2);
+  }
+  if (sc.zero) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[k][j] = make_float2(0.0f, 0.0f);
   }
 }
 
@@ -1292,11 +1350,11 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       if (MX) {
         scale_rows_16th(v);
         quantize_mx<true>(v, q);
+        scale_by_16th(q.S);
+        dequantize(q.code, q.S, v, T.negzero);
       } else {
-        quantize<G, true, true>(v, q);
+        quantize_decode<G, true, true>(v, 0.0625f, T.negzero);
       }
-      scale_by_16th(q.S);
-      dequantize(q.code, q.S, v, T.negzero);
       rows_bfly(v, 2);
       rows_bfly(v, 1);
       transpose_half<false>(v, xa);
@@ -1304,8 +1362,12 @@ roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       rows_bfly(v, 1);
       level1_inv(v);
     } else {
-      if (MX) quantize_mx<false>(v, q); else quantize<G, false, false>(v, q);
-      dequantize(q.code, q.S, v, T.negzero);
+      if (MX) {
+        quantize_mx<false>(v, q);
+        dequantize(q.code, q.S, v, T.negzero);
+      } else {
+        quantize_decode<G, false, false>(v, 1.0f, T.negzero);
+      }
       staging_free();
     }
     if (XF) tile_write_f32(ws.xbuf, blk, l4, v); else tile_write_bf16(ws.xbuf, blk, l4, v);
