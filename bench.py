@@ -54,7 +54,7 @@ L2_FLUSH_BYTES = 512 << 20
 L2_POLICY = (f"flushed between steps and before every per-config launch ({L2_FLUSH_BYTES >> 20} MiB write + "
              f"{L2_FLUSH_BYTES >> 20} MiB read, outside the timed events); headline tensors are also larger than L2")
 REF_SAMPLE = 1 << 26                 # elements of each reference-arm step (a sample of the workload)
-CPU_SAMPLE = 1 << 24                 # elements of each cpu_baseline repetition
+CPU_SAMPLE = REF_SAMPLE              # elements of each cpu_baseline repetition (the same sample)
 TARGET_FRAC = 0.70
 TARGET_MIN_BYTES = 64 << 20          # the target applies to workloads of at least 64 MiB of BF16
 
