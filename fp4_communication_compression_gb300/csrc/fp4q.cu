@@ -1864,7 +1864,7 @@ fp4q_status check_params(const fp4q_params* p, int& G, int& fwht, bool& mx) {
   if (p) d = *p;
   if ((d.group != 16 && d.group != 32) || d.block != FP4Q_BLOCK || d.fwht < 0 || d.fwht > 2 ||
       (d.scales != FP4Q_SCALES_DUAL && d.scales != FP4Q_SCALES_E8M0) ||
-      (d.scales == FP4Q_SCALES_E8M0 && d.group != 32) || (d.fwht == 2 && d.scales != FP4Q_SCALES_DUAL))
+      (d.scales == FP4Q_SCALES_E8M0 && d.group != 32))
     return FP4Q_ERR_PARAM;
   G = d.group;
   fwht = d.fwht;
@@ -1927,14 +1927,14 @@ fp4q_status launch_compress(const void* x, int64_t n, const Payload& P, cudaStre
 // Tensor-core compress (fwht = 2): full blocks through compress_tc_kernel, persistent, one CTA
 // per SM (its TMEM allocation is the SM's 512 columns); a last partial block through the
 // one-warp tail kernel with the butterfly transform.
-template <int G>
+template <int G, bool MX>
 fp4q_status launch_compress_tc(const void* x, int64_t n, const Payload& P, cudaStream_t s) {
   const int64_t nfull = n / FP4Q_BLOCK * FP4Q_BLOCK;
   if (nfull > 0) {
     const int64_t nb = nfull / FP4Q_BLOCK, batches = (nb + kTcBatchBlocks - 1) / kTcBatchBlocks;
     CUtensorMap xm;   // 128-byte lines (quarter-blocks), boxes of 256 lines (64 blocks), two per batch
     if (!line_map(&xm, x, nfull, false, 2 * kTcBatchBlocks)) return FP4Q_ERR_CUDA;
-    auto k = compress_tc_kernel<G>;
+    auto k = compress_tc_kernel<G, MX>;
     Launch L;
     // plan() sizes the grid as (units / warps) CTAs: one unit per warp and batch gives one CTA
     // per batch, capped at one per SM
@@ -1945,7 +1945,7 @@ fp4q_status launch_compress_tc(const void* x, int64_t n, const Payload& P, cudaS
   }
   if (n == nfull) return FP4Q_OK;
   const void* xt = static_cast<const uint8_t*>(x) + nfull * 2;
-  return launch_tail(tail_compress_kernel<G, 1, false, false>, s, xt, (int)(n - nfull), P, (int64_t)(nfull / FP4Q_BLOCK));
+  return launch_tail(tail_compress_kernel<G, 1, MX, false>, s, xt, (int)(n - nfull), P, (int64_t)(nfull / FP4Q_BLOCK));
 }
 
 template <int G, int F, int DT, int B, bool MX>
@@ -2101,9 +2101,10 @@ fp4q_status dispatch_decompress(int key, const Payload& payload, int64_t n, void
 
 template <bool XF>
 fp4q_status dispatch_compress(int G, int F, bool MX, const void* x, int64_t n, const Payload& P, cudaStream_t s) {
-  if (F == 2) {   // tensor-core transform: BF16 input, dual scales (check_params rejects E8M0)
+  if (F == 2) {   // tensor-core transform: BF16 input
     if (XF) return FP4Q_ERR_PARAM;
-    return G == 16 ? launch_compress_tc<16>(x, n, P, s) : launch_compress_tc<32>(x, n, P, s);
+    if (MX) return launch_compress_tc<32, true>(x, n, P, s);
+    return G == 16 ? launch_compress_tc<16, false>(x, n, P, s) : launch_compress_tc<32, false>(x, n, P, s);
   }
   if (MX) return F ? launch_compress<32, 1, true, XF>(x, n, P, s) : launch_compress<32, 0, true, XF>(x, n, P, s);
   if (G == 16) return F ? launch_compress<16, 1, false, XF>(x, n, P, s) : launch_compress<16, 0, false, XF>(x, n, P, s);

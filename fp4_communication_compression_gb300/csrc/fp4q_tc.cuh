@@ -17,8 +17,8 @@
 // lane (block, gh') then holds the 64 values (gl, p) of that quarter-block after the mixing;
 // its thread loads them with tcgen05.ld, applies H4 across gl and H16 along p with FP32
 // butterflies and holds the four groups 4 gh' + gl' of the block: the row layout of the
-// tiled kernels (four lanes per block, four groups per lane), so the same quantisation and
-// store run on it.
+// tiled kernels (four lanes per block, four groups per lane), so the same quantisation (dual
+// or E8M0 scales) and store run on it.
 //
 // The products are exact (BF16 times +-1) but the tensor core accumulates each 4-term sum in
 // its own order and the stages run in another order than the contract's butterfly sequence,
@@ -114,7 +114,7 @@ __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, const vol
   return false;
 }
 
-template <int G>
+template <int G, bool MX>
 __global__ void __launch_bounds__(kTcThreads, 1)
 compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t nb, int64_t batches) {
   extern __shared__ uint8_t smem_raw[];
@@ -267,9 +267,14 @@ compress_tc_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, int64_t 
         for (int j = 0; j < 8; ++j) bfly_in(v[k][j]);
       level1_fwd_from2(v);
       Quant q;
-      quantize<G, false, true>(v, q);
+      if (MX) {
+        scale_rows_16th(v);                     // the power-of-two scale sees y itself
+        quantize_mx<false>(v, q);
+      } else {
+        quantize<G, false, true>(v, q);
+      }
       const int64_t gb = (first + i * step) * kTcBatchBlocks + kTcSubBlocks * grp + 8 * wq + (lane >> 2);
-      if (gb < nb) store_block<G, false, false>(P, gb, l4, q);
+      if (gb < nb) store_block<G, false, MX>(P, gb, l4, q);
     }
   }
   tc_fence_before();

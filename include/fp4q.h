@@ -74,7 +74,7 @@
  *            of the block maximum), so a scale
  *            or a code whose contract value lies on a rounding boundary can differ; the
  *            payload format is unchanged and decodes as an fwht = 1 payload. Contiguous
- *            BF16 input and dual scales only (fp4q_compress, fp4q_compress_segments); the
+ *            BF16 input only, either scale format (fp4q_compress, fp4q_compress_segments); the
  *            decoders and the reduce accept fwht = 2 as fwht = 1; the other producers reject
  *            it (FP4Q_ERR_PARAM).
  *
@@ -127,7 +127,7 @@ typedef enum fp4q_status {
   FP4Q_ERR_SIZE = 2,     /* n <= 0 or n >= 2^37                                         */
   FP4Q_ERR_ALIGN = 3,    /* a data pointer is not 16-byte aligned                       */
   FP4Q_ERR_PARAM = 4,    /* bad params: group not 16/32, block not 256, fwht not 0/1/2,
-                            scales not 0/1, E8M0 with group != 32 or fwht 2, R outside [1, 8],
+                            scales not 0/1 or E8M0 with group != 32, R outside [1, 8],
                             unknown dtype, beta not 0/1                                 */
   FP4Q_ERR_OVERLAP = 5,  /* an output buffer overlaps an input buffer                   */
   FP4Q_ERR_CUDA = 6      /* a CUDA runtime call or a kernel launch failed               */

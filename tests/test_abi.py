@@ -80,9 +80,9 @@ def test_payload_bytes_defaults_and_invalid(L):
     assert L.fp4q_payload_bytes(4096 + 1, None) == L.fp4q_payload_bytes(4096 + 256, None)
     for g, b, f in [(8, 256, 1), (16, 128, 1), (16, 256, 3), (64, 256, 0)]:
         assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(g, b, f))) == 0
-    # fwht = 2 (the tensor-core encoder) writes the dual-scale format only
+    # fwht = 2 (the tensor-core encoder) writes either payload format
     assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(16, 256, 2))) == 2368
-    assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(32, 256, 2, 1))) == 0
+    assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(32, 256, 2, 1))) == 2048 + 128
     # E8M0 scales need group 32; unknown scale formats are rejected
     for g, sc in [(16, 1), (32, 2), (32, -1), (16, 7)]:
         assert L.fp4q_payload_bytes(4096, ctypes.byref(_lib.Params(g, 256, 1, sc))) == 0
@@ -265,7 +265,7 @@ def test_tensor_core_encoder_argument_errors(L):
     assert L.fp4q_roundtrip_f32(A, 4096, B, p2, None) == _lib.ERR_PARAM
     assert L.fp4q_compress_2d(A, 4, 512, 1024, B, p2, None) == _lib.ERR_PARAM
     assert L.fp4q_roundtrip_2d(A, 4, 512, 1024, B, 1024, p2, None) == _lib.ERR_PARAM
-    assert L.fp4q_compress(A, 4096, B, ctypes.byref(_lib.Params(32, 256, 2, 1)), None) == _lib.ERR_PARAM
+    assert L.fp4q_compress(A, 4096, None, ctypes.byref(_lib.Params(32, 256, 2, 1)), None) == _lib.ERR_NULL
     # decoders: fwht = 2 passes the parameter check (these calls then stop at a host check)
     assert L.fp4q_decompress_accumulate(A, 4096, B + 4, _lib.BF16, 1, p2, None) == _lib.ERR_ALIGN
     assert L.fp4q_decompress_accumulate_2d(A, 4, 512, B + 4, 1024, _lib.BF16, 1, p2, None) == _lib.ERR_ALIGN
