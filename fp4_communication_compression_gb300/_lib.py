@@ -8,6 +8,7 @@ raises ``RuntimeError``.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
 import platform
 import subprocess
@@ -57,17 +58,28 @@ class Segments(ctypes.Structure):
 
 def build(force: bool = False, nvcc: str = "nvcc") -> str:
     """Compile csrc/fp4q.cu for sm_103a into the package directory; returns the .so path."""
+    # up to date when the library was built from exactly these sources and flags (a content
+    # hash, not file times: a copied tree keeps neither order nor clock of the original)
     csrc = os.path.dirname(_SRC)
-    deps = [_HDR] + [os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh"))]
-    newest = max(os.path.getmtime(f) for f in deps)
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
-        return LIB_PATH
+    deps = [_HDR] + sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
+    h = hashlib.sha256(" ".join([nvcc, *NVCC_FLAGS]).encode())
+    for f in deps:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    stamp = LIB_PATH + ".sha256"
+    if not force and os.path.exists(LIB_PATH) and os.path.exists(stamp):
+        with open(stamp) as fh:
+            if fh.read().strip() == h.hexdigest():
+                return LIB_PATH
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     cmd = [nvcc, *NVCC_FLAGS, "-I", os.path.dirname(_HDR), _SRC, "-o", tmp]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
     os.replace(tmp, LIB_PATH)
+    with open(stamp + f".tmp{os.getpid()}", "w") as fh:
+        fh.write(h.hexdigest())
+    os.replace(stamp + f".tmp{os.getpid()}", stamp)
     return LIB_PATH
 
 

@@ -8,6 +8,7 @@ with the CUDA library and never imports it.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
 import platform
 import subprocess
@@ -26,15 +27,24 @@ BLOCK = 256
 
 def build(force: bool = False) -> str:
     """Compile the oracle into a shared library next to its source and return its path."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
-        return _LIB
-    tmp = _LIB + f".tmp{os.getpid()}"
     base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+    # up to date when built from exactly this source (a content hash, not file times)
+    with open(_SRC, "rb") as fh:
+        digest = hashlib.sha256(" ".join(base).encode() + b"\0" + fh.read()).hexdigest()
+    stamp = _LIB + ".sha256"
+    if not force and os.path.exists(_LIB) and os.path.exists(stamp):
+        with open(stamp) as fh:
+            if fh.read().strip() == digest:
+                return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
     try:
         subprocess.run(base + ["-fopenmp", _SRC, "-lm", "-o", tmp], check=True, capture_output=True)
     except subprocess.CalledProcessError:
         subprocess.run(base + [_SRC, "-lm", "-o", tmp], check=True, capture_output=True)
     os.replace(tmp, _LIB)
+    with open(stamp + f".tmp{os.getpid()}", "w") as fh:
+        fh.write(digest)
+    os.replace(stamp + f".tmp{os.getpid()}", stamp)
     return _LIB
 
 
