@@ -80,6 +80,16 @@ constexpr int kReduceWarps = 4;
 // measured finishing up to 9 us apart under the round-robin assignment.
 constexpr int kReduceDynWarps = 16;
 constexpr int64_t kReduceDynTilesPerSm = 384;
+// Compress and roundtrip of BF16 input with at least kCompressDynTilesPerWarp tiles per warp
+// run the same way: one CTA of kCompressDynWarps warps (the 5 x 4 warps as one CTA) per SM,
+// tiles claimed dynamically. The five CTAs of an SM were measured finishing up to 12 us apart
+// at 2^26 elements (the warps of one CTA within 1 us), the SM's last stretch running on few
+// warps; claimed dynamically they end within 2 us (compress 38.9 -> 37.4 us at 2^26, 69.6 ->
+// 67.7 at 2^27; roundtrip 61.4 -> 59.4, 113.5 -> 110.1). Below 8 tiles per warp it gained
+// nothing, and for the reduce below 384 tiles per SM it lost (R = 8 at 2^25: 47.2 -> 54.9 us).
+constexpr int kCompressDynWarps = 20;
+constexpr int64_t kCompressDynTilesPerWarp = 8;
+constexpr int kDynHeaderBytes = 2048;      // barriers of up to 31 warps, the claim counter last
 constexpr float kZeroLimit = 2688.0f * 0x1p-100f;   // all-zero block guard on A_b
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -860,23 +870,28 @@ constexpr int kHeaderBytes = 1024;         // per-CTA header: every warp's stage
 // CTA shared memory: [alignment slack][header: 64 bytes of barriers per warp][warp regions],
 // each warp region = [input stages][xbuf of XB bytes], 1024-byte aligned (the 128-byte TMA
 // swizzle repeats every 1024 bytes).
-template <int WARPS, int STAGES, int IN_BYTES, int XB = kXBufBytes>
+template <int WARPS, int STAGES, int IN_BYTES, int XB = kXBufBytes, int HDR = kHeaderBytes>
 struct WarpSmemLayout {
   static constexpr int kRegion = STAGES * IN_BYTES + XB;
   static_assert(kRegion % 1024 == 0, "warp regions must stay 1024-byte aligned");
-  static constexpr int kCtaBytes = 1024 + kHeaderBytes + WARPS * kRegion;
+  static_assert(64 * WARPS <= HDR - 8, "the header holds 64 bytes of barriers per warp");
+  static constexpr int kCtaBytes = 1024 + HDR + WARPS * kRegion;
 };
+// Shared address of a DYN CTA's claim counter: the last word of its header.
+__device__ __forceinline__ uint32_t dyn_counter_addr(uint8_t* raw) {
+  return ((smem_addr(raw) + 1023u) & ~1023u) + (uint32_t)kDynHeaderBytes - 8u;
+}
 
 struct WarpSmem {
   uint32_t stage0, xbuf, bar0;
 };
 
-template <int STAGES, int IN_BYTES, int XB = kXBufBytes>
+template <int STAGES, int IN_BYTES, int XB = kXBufBytes, int HDR = kHeaderBytes>
 __device__ __forceinline__ WarpSmem warp_smem(uint8_t* raw, int warp) {
   constexpr int region = STAGES * IN_BYTES + XB;
   const uint32_t base = (smem_addr(raw) + 1023u) & ~1023u;
   WarpSmem w;
-  w.stage0 = base + kHeaderBytes + (uint32_t)(warp * region);
+  w.stage0 = base + HDR + (uint32_t)(warp * region);
   w.xbuf = w.stage0 + STAGES * IN_BYTES;
   w.bar0 = base + 64u * (uint32_t)warp;
   return w;
@@ -1213,20 +1228,29 @@ __device__ __forceinline__ void staging_store(const CUtensorMap* map, const Tile
 
 // K1: compress. x (bfloat16, n) -> payload. Input tiles arrive by TMA.
 // XF: FP32 input (8 KiB tiles of 64 lines) instead of BF16 (4 KiB, 32 lines).
-template <int G, int FWHT, bool MX, bool XF>
-__global__ void __launch_bounds__(kCompressWarps * 32, XF ? kCompressCtasF32 : kCompressCtas)
+// DYN: one CTA of kCompressDynWarps warps per SM claiming its tiles dynamically (InPipe DYN).
+template <int G, int FWHT, bool MX, bool XF, bool DYN = false>
+__global__ void __launch_bounds__(DYN ? kCompressDynWarps * 32 : kCompressWarps * 32,
+                                  DYN ? 1 : (XF ? kCompressCtasF32 : kCompressCtas))
 compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T) {
   constexpr int IN = XF ? 8192 : 4096;
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  const WarpSmem ws = warp_smem<kCompressStages, IN, kCompressXBytes>(smem_raw, warp);
+  const WarpSmem ws = warp_smem<kCompressStages, IN, kCompressXBytes, DYN ? kDynHeaderBytes : kHeaderBytes>(smem_raw, warp);
   const XposeHalf xa = xpose_half_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<XF ? 8 : 4>(&xmap, T, t, buf, bar, lane); };
-  InPipe<kCompressStages, IN, true> pipe{};
-  pipe.start(ws.stage0, ws.bar0, warp_global<kCompressWarps>(), warp_count<kCompressWarps>(), T.tiles, lane, issue);
-  for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
+  InPipe<kCompressStages, IN, true, DYN> pipe{};
+  if constexpr (DYN) {
+    const uint32_t ctr = dyn_counter_addr(smem_raw);
+    dyn_counter_init(ctr);
+    pipe.start_dyn(ws.stage0, ws.bar0, ctr, T.tiles, lane, issue);
+  } else {
+    pipe.start(ws.stage0, ws.bar0, warp_global<kCompressWarps>(), warp_count<kCompressWarps>(), T.tiles, lane, issue);
+  }
+  for (int64_t t = DYN ? pipe.tile() : pipe.t0; t < T.tiles; t = DYN ? pipe.tile() : t + pipe.W) {
+    pipe.ask(lane);
     const int64_t gb = t * kTileBlocks + blk;
     const bool valid = gb < T.nb;
     if (!pipe.wait()) return;
@@ -1319,21 +1343,31 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
 
 // K3: fused roundtrip. x (bfloat16) -> y = bf16(decode(compress(x))), no payload.
 // XF: FP32 input and output instead of BF16.
-template <int G, int FWHT, bool MX, bool XF>
-__global__ void __launch_bounds__(kRoundtripWarps * 32, XF ? kRoundtripCtasF32 : kRoundtripCtas)
+// DYN: one CTA of kCompressDynWarps warps per SM claiming its tiles dynamically (as compress).
+template <int G, int FWHT, bool MX, bool XF, bool DYN = false>
+__global__ void __launch_bounds__(DYN ? kCompressDynWarps * 32 : kRoundtripWarps * 32,
+                                  DYN ? 1 : (XF ? kRoundtripCtasF32 : kRoundtripCtas))
 roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap, TileLoop T) {
   constexpr int IN = XF ? 8192 : 4096;
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  const WarpSmem ws = warp_smem<kRoundtripStages, IN, RoundtripXBytes<XF>::value>(smem_raw, warp);
+  const WarpSmem ws =
+      warp_smem<kRoundtripStages, IN, RoundtripXBytes<XF>::value, DYN ? kDynHeaderBytes : kHeaderBytes>(smem_raw, warp);
   const XposeHalf xa = xpose_half_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<XF ? 8 : 4>(&xmap, T, t, buf, bar, lane); };
-  InPipe<kRoundtripStages, IN, true> pipe{};
-  pipe.start(ws.stage0, ws.bar0, warp_global<kRoundtripWarps>(), warp_count<kRoundtripWarps>(), T.tiles, lane,
-             issue);
-  for (int64_t t = pipe.t0; t < T.tiles; t += pipe.W) {
+  InPipe<kRoundtripStages, IN, true, DYN> pipe{};
+  if constexpr (DYN) {
+    const uint32_t ctr = dyn_counter_addr(smem_raw);
+    dyn_counter_init(ctr);
+    pipe.start_dyn(ws.stage0, ws.bar0, ctr, T.tiles, lane, issue);
+  } else {
+    pipe.start(ws.stage0, ws.bar0, warp_global<kRoundtripWarps>(), warp_count<kRoundtripWarps>(), T.tiles, lane,
+               issue);
+  }
+  for (int64_t t = DYN ? pipe.tile() : pipe.t0; t < T.tiles; t = DYN ? pipe.tile() : t + pipe.W) {
+    pipe.ask(lane);
     if (!pipe.wait()) break;
     Rows v;
     tile_read_in<XF, FWHT != 0>(pipe.cur(), blk, l4, v);
@@ -1911,12 +1945,28 @@ fp4q_status launch_compress(const void* x, int64_t n, const Payload& P, cudaStre
     TileLoop T = tiles_of(nfull);
     CUtensorMap xm;
     if (!line_map(&xm, x, nfull, XF)) return FP4Q_ERR_CUDA;
-    auto k = compress_kernel<G, F, MX, XF>;
-    Launch L;
-    fp4q_status st = plan(k, kCompressWarps,
-                          WarpSmemLayout<kCompressWarps, kCompressStages, XF ? 8192 : 4096, kCompressXBytes>::kCtaBytes, T.tiles, L,
-                          small_grid_cap(T.tiles, kCompressWarps, kCompressCtas));
-    if (st == FP4Q_OK) st = launch_pdl(k, L, kCompressWarps * 32, s, xm, P, T);
+    const int sms = num_sms();
+    fp4q_status st = FP4Q_OK;
+    bool dyn = false;
+    if constexpr (!XF) {
+      dyn = sms > 0 && T.tiles >= kCompressDynTilesPerWarp * kCompressDynWarps * sms;
+      if (dyn) {
+        auto k = compress_kernel<G, F, MX, false, true>;
+        Launch L;
+        st = plan(k, kCompressDynWarps,
+                  WarpSmemLayout<kCompressDynWarps, kCompressStages, 4096, kCompressXBytes, kDynHeaderBytes>::kCtaBytes,
+                  T.tiles, L, 1);
+        if (st == FP4Q_OK) st = launch_pdl(k, L, kCompressDynWarps * 32, s, xm, P, T);
+      }
+    }
+    if (!dyn) {
+      auto k = compress_kernel<G, F, MX, XF>;
+      Launch L;
+      st = plan(k, kCompressWarps,
+                WarpSmemLayout<kCompressWarps, kCompressStages, XF ? 8192 : 4096, kCompressXBytes>::kCtaBytes, T.tiles, L,
+                small_grid_cap(T.tiles, kCompressWarps, kCompressCtas));
+      if (st == FP4Q_OK) st = launch_pdl(k, L, kCompressWarps * 32, s, xm, P, T);
+    }
     if (st != FP4Q_OK) return st;
   }
   if (n == nfull) return FP4Q_OK;
@@ -1977,12 +2027,29 @@ fp4q_status launch_roundtrip(const void* x, int64_t n, void* y, cudaStream_t s) 
     TileLoop T = tiles_of(nfull);
     CUtensorMap xm, ym;
     if (!line_map(&xm, x, nfull, XF) || !line_map(&ym, y, nfull, XF)) return FP4Q_ERR_CUDA;
-    auto k = roundtrip_kernel<G, F, MX, XF>;
-    Launch L;
-    fp4q_status st = plan(k, kRoundtripWarps,
-                          WarpSmemLayout<kRoundtripWarps, kRoundtripStages, XF ? 8192 : 4096, RoundtripXBytes<XF>::value>::kCtaBytes,
-                          T.tiles, L, XF ? 0 : small_grid_cap(T.tiles, kRoundtripWarps, kRoundtripCtas));
-    if (st == FP4Q_OK) st = launch_pdl(k, L, kRoundtripWarps * 32, s, xm, ym, T);
+    const int sms = num_sms();
+    fp4q_status st = FP4Q_OK;
+    bool dyn = false;
+    if constexpr (!XF) {
+      dyn = sms > 0 && T.tiles >= kCompressDynTilesPerWarp * kCompressDynWarps * sms;
+      if (dyn) {
+        auto k = roundtrip_kernel<G, F, MX, false, true>;
+        Launch L;
+        st = plan(k, kCompressDynWarps,
+                  WarpSmemLayout<kCompressDynWarps, kRoundtripStages, 4096, RoundtripXBytes<false>::value,
+                                 kDynHeaderBytes>::kCtaBytes,
+                  T.tiles, L, 1);
+        if (st == FP4Q_OK) st = launch_pdl(k, L, kCompressDynWarps * 32, s, xm, ym, T);
+      }
+    }
+    if (!dyn) {
+      auto k = roundtrip_kernel<G, F, MX, XF>;
+      Launch L;
+      st = plan(k, kRoundtripWarps,
+                WarpSmemLayout<kRoundtripWarps, kRoundtripStages, XF ? 8192 : 4096, RoundtripXBytes<XF>::value>::kCtaBytes,
+                T.tiles, L, XF ? 0 : small_grid_cap(T.tiles, kRoundtripWarps, kRoundtripCtas));
+      if (st == FP4Q_OK) st = launch_pdl(k, L, kRoundtripWarps * 32, s, xm, ym, T);
+    }
     if (st != FP4Q_OK) return st;
   }
   if (n == nfull) return FP4Q_OK;
