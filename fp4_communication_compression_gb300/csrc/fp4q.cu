@@ -76,10 +76,12 @@ constexpr int kDecompressWarps = 4, kDecompressStages = 1, kDecompressCtas = 4;
 constexpr int kDecompressGridCtas = 4;     // resident CTAs per SM the grid is sized for
 constexpr int kReduceWarps = 4;
 // Large reduces (at least kReduceDynTilesPerSm tiles per SM) run one CTA of
-// kReduceDynWarps warps per SM with dynamic tile claims (InPipe DYN): warps of one SM were
+// ReduceCfg<R>::kDynWarps warps per SM with dynamic tile claims (InPipe DYN): warps of one SM were
 // measured finishing up to 9 us apart under the round-robin assignment.
-constexpr int kReduceDynWarps = 16;
 constexpr int64_t kReduceDynTilesPerSm = 384;
+// R <= 2 (two stages, 20-warp CTAs) already gains from 8 tiles per warp (R = 2: 35.0 -> 33.0 us
+// at 2^26, 59.9 -> 57.7 us at 2^27, equal at 2^25); R = 8 lost there (45.2 -> 53.6 us at 2^25)
+constexpr int64_t kReduceDynTilesPerWarpR2 = 8;
 // Compress and roundtrip of BF16 input with at least kCompressDynTilesPerWarp tiles per warp
 // run the same way: one CTA of kCompressDynWarps warps (the 5 x 4 warps as one CTA) per SM,
 // tiles claimed dynamically. The five CTAs of an SM were measured finishing up to 12 us apart
@@ -1446,6 +1448,8 @@ struct ReduceCfg {
   // variants prefetch every rank's scales into registers and keep 4 (at 5 they spill: R = 4
   // went from 29.4 to 36.8 us)
   static constexpr int kMinCtas = (R == 3 || R == 4) ? 4 : 5;
+  // dynamic-claim CTAs (InPipe DYN) hold as many warps as that fixed grid has per SM
+  static constexpr int kDynWarps = 4 * kMinCtas;
   static constexpr int cta_bytes(int warps) { return warps * kRegion + 128 + 16; }   // + DYN counter
   static constexpr int kStageBytes = R * kRankStageBytes;
   static constexpr int kRegion = kStagesR * kStageBytes + 128;       // + barriers
@@ -1453,7 +1457,7 @@ struct ReduceCfg {
 };
 
 template <int G, int R, bool MX, bool DYN>
-__global__ void __launch_bounds__(DYN ? kReduceDynWarps * 32 : kReduceWarps * 32, DYN ? 1 : ReduceCfg<R>::kMinCtas)
+__global__ void __launch_bounds__(DYN ? ReduceCfg<R>::kDynWarps * 32 : kReduceWarps * 32, DYN ? 1 : ReduceCfg<R>::kMinCtas)
 reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
   typedef ReduceCfg<R> C;
   constexpr bool DS = C::kDirectScales && !MX;
@@ -1507,7 +1511,7 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
   };
   InPipe<C::kStagesR, C::kStageBytes, true, DYN> pipe{};
   if constexpr (DYN) {
-    const uint32_t ctr = ((smem_addr(smem_raw) + 127u) & ~127u) + (uint32_t)(kReduceDynWarps * C::kRegion);
+    const uint32_t ctr = ((smem_addr(smem_raw) + 127u) & ~127u) + (uint32_t)(C::kDynWarps * C::kRegion);
     dyn_counter_init(ctr);
     pipe.start_dyn(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), ctr, T.tiles, lane, issue);
   } else {
@@ -2117,9 +2121,10 @@ fp4q_status launch_reduce_r(const RankPtrs& in, int64_t n, const Payload& P, cud
   n = padded_n(n);   // the reduce works on whole (zero-padded) blocks of the payloads
   TileLoop T = tiles_of(n);
   const int sms = num_sms();
-  const bool dyn = sms > 0 && T.tiles >= kReduceDynTilesPerSm * sms;
+  const int64_t dyn_min = R <= 2 ? kReduceDynTilesPerWarpR2 * ReduceCfg<R>::kDynWarps : kReduceDynTilesPerSm;
+  const bool dyn = sms > 0 && T.tiles >= dyn_min * sms;
   auto k = dyn ? reduce_kernel<G, R, MX, true> : reduce_kernel<G, R, MX, false>;
-  const int warps = dyn ? kReduceDynWarps : kReduceWarps;
+  const int warps = dyn ? ReduceCfg<R>::kDynWarps : kReduceWarps;
   Launch L;
   fp4q_status st = plan(k, warps, ReduceCfg<R>::cta_bytes(warps), T.tiles, L);
   if (st != FP4Q_OK) return st;
