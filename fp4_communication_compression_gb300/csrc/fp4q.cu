@@ -90,6 +90,9 @@ constexpr int64_t kReduceDynTilesPerWarpR2 = 8;
 // 67.7 at 2^27; roundtrip 61.4 -> 59.4, 113.5 -> 110.1). Below 8 tiles per warp it gained
 // nothing, and for the reduce below 384 tiles per SM it lost (R = 8 at 2^25: 47.2 -> 54.9 us).
 constexpr int kCompressDynWarps = 20;
+// Decompress-accumulate into BF16 with beta = 1 likewise (its 4 CTAs x 4 warps as one CTA):
+// 48.2 -> 47.0 us at 2^26, 96.2 -> 95.7 us at 2^27, equal at 2^28 - 2^29.
+constexpr int kDecompressDynWarps = 16;
 constexpr int64_t kCompressDynTilesPerWarp = 8;
 constexpr int kDynHeaderBytes = 2048;      // barriers of up to 31 warps, the claim counter last
 constexpr float kZeroLimit = 2688.0f * 0x1p-100f;   // all-zero block guard on A_b
@@ -985,6 +988,8 @@ struct InPipe {
   __device__ __forceinline__ void ask(int lane) {
     if (DYN) asked = claim_ask(lane);
   }
+  // DYN: the tile that claim is for (every lane; the next refill loads it).
+  __device__ __forceinline__ int64_t asked_tile() const { return claim_tile(asked); }
   __device__ __forceinline__ uint32_t cur() const { return buf(i % STAGES); }
   // Wait for the current tile. On failure record the fault, wait (bounded) for every copy
   // still in flight into this warp's stages, and return false: the caller must stop.
@@ -1284,9 +1289,13 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
 // K2: decompress-accumulate. payload -> dst (dtype DT), dst = BETA ? dst + x^ : x^.
 // The payload of the next tile is prefetched into registers; dst tiles are read (BETA) and
 // written through the swizzled shared staging buffer by TMA.
-template <int G, int FWHT, int DT, int BETA, bool MX>
-__global__ void __launch_bounds__(kDecompressWarps * 32, kDecompressCtas)
+// DYN (BF16 dst, BETA = 1): one CTA of kDecompressDynWarps warps per SM claiming its tiles
+// dynamically; the payload prefetch follows the claims (the tile claimed at the top of an
+// iteration is the one the refill loads next).
+template <int G, int FWHT, int DT, int BETA, bool MX, bool DYN = false>
+__global__ void __launch_bounds__(DYN ? kDecompressDynWarps * 32 : kDecompressWarps * 32, DYN ? 1 : kDecompressCtas)
 decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop T) {
+  static_assert(!DYN || (BETA && DT == FP4Q_BF16), "dynamic claims ride on the destination pipeline");
   constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
   constexpr int LPB = DT == FP4Q_BF16 ? 4 : 8;   // 128-byte lines per block of dst
   constexpr bool LB = FWHT != 0;
@@ -1294,17 +1303,34 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
-  const WarpSmem ws = warp_smem<kDecompressStages, BETA ? TB : 0>(smem_raw, warp);
+  const WarpSmem ws = warp_smem<kDecompressStages, BETA ? TB : 0, kXBufBytes, DYN ? kDynHeaderBytes : kHeaderBytes>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<LPB>(&dmap, T, t, buf, bar, lane); };
-  InPipe<kDecompressStages, TB, true> pipe{};
-  const int64_t t0 = warp_global<kDecompressWarps>(), W = warp_count<kDecompressWarps>();
-  if (BETA) pipe.start(ws.stage0, ws.bar0, t0, W, T.tiles, lane, issue);
+  InPipe<kDecompressStages, TB, true, DYN> pipe{};
+  int64_t t0, W;
+  if constexpr (DYN) {
+    const uint32_t ctr = dyn_counter_addr(smem_raw);
+    dyn_counter_init(ctr);
+    pipe.start_dyn(ws.stage0, ws.bar0, ctr, T.tiles, lane, issue);
+    t0 = pipe.tile();
+    W = 0;
+  } else {
+    t0 = warp_global<kDecompressWarps>();
+    W = warp_count<kDecompressWarps>();
+    if (BETA) pipe.start(ws.stage0, ws.bar0, t0, W, T.tiles, lane, issue);
+  }
   PayRaw cur, nxt;
   if (t0 < T.tiles && t0 * kTileBlocks + blk < T.nb) pay_load<G, LB, MX>(P, t0 * kTileBlocks + blk, l4, cur);
   else pay_zero(cur);
-  for (int64_t t = t0; t < T.tiles; t += W) {
-    const int64_t tn = t + W, gbn = tn * kTileBlocks + blk;
+  for (int64_t t = t0; t < T.tiles; t = DYN ? pipe.tile() : t + W) {
+    int64_t tn;
+    if constexpr (DYN) {
+      pipe.ask(lane);
+      tn = pipe.asked_tile();
+    } else {
+      tn = t + W;
+    }
+    const int64_t gbn = tn * kTileBlocks + blk;
     if (tn < T.tiles && gbn < T.nb) pay_load<G, LB, MX>(P, gbn, l4, nxt); else pay_zero(nxt);
     float S[4];
     pay_scales<G, LB, MX>(cur, l4, S);
@@ -2009,13 +2035,28 @@ fp4q_status launch_decompress(const Payload& P, int64_t n, void* dst, cudaStream
     TileLoop T = tiles_of(nfull);
     CUtensorMap dm;
     if (!line_map(&dm, dst, nfull, DT == FP4Q_F32)) return FP4Q_ERR_CUDA;
-    auto k = decompress_kernel<G, F, DT, B, MX>;
     constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
-    Launch L;
-    fp4q_status st = plan(k, kDecompressWarps,
-                          WarpSmemLayout<kDecompressWarps, kDecompressStages, B ? TB : 0>::kCtaBytes, T.tiles, L,
-                          kDecompressGridCtas);
-    if (st == FP4Q_OK) st = launch_pdl(k, L, kDecompressWarps * 32, s, dm, P, T);
+    const int sms = num_sms();
+    fp4q_status st = FP4Q_OK;
+    bool dyn = false;
+    if constexpr (DT == FP4Q_BF16 && B == 1) {
+      dyn = sms > 0 && T.tiles >= kCompressDynTilesPerWarp * kDecompressDynWarps * sms;
+      if (dyn) {
+        auto k = decompress_kernel<G, F, DT, B, MX, true>;
+        Launch L;
+        st = plan(k, kDecompressDynWarps,
+                  WarpSmemLayout<kDecompressDynWarps, kDecompressStages, TB, kXBufBytes, kDynHeaderBytes>::kCtaBytes,
+                  T.tiles, L, 1);
+        if (st == FP4Q_OK) st = launch_pdl(k, L, kDecompressDynWarps * 32, s, dm, P, T);
+      }
+    }
+    if (!dyn) {
+      auto k = decompress_kernel<G, F, DT, B, MX>;
+      Launch L;
+      st = plan(k, kDecompressWarps, WarpSmemLayout<kDecompressWarps, kDecompressStages, B ? TB : 0>::kCtaBytes, T.tiles,
+                L, kDecompressGridCtas);
+      if (st == FP4Q_OK) st = launch_pdl(k, L, kDecompressWarps * 32, s, dm, P, T);
+    }
     if (st != FP4Q_OK) return st;
   }
   if (n == nfull) return FP4Q_OK;
