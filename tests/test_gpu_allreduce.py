@@ -130,3 +130,47 @@ def test_two_process_allreduce_matches_oracle(dev, n, kw):
     for r in range(world):
         assert res[r][1] == 0, f"rank {r}: fault word set"
         assert np.array_equal(res[r][0], want), f"rank {r} differs from the oracle's unsharded reduce"
+
+
+def _nccl_worker(port, n, kw, q):
+    import torch.distributed as dist
+    from fp4_communication_compression_gb300.allreduce import CompressedAllReduce
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), NCCL_NVLS_ENABLE="0")
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=dev)
+    try:
+        x, d0 = _rank_inputs(n, 0)
+        ar = CompressedAllReduce(n, dev, **kw)
+        assert ar.staging == "device"
+        xt = inputs.bits_to_torch(x, dev)
+        for _ in range(2):
+            dst = inputs.bits_to_torch(d0, dev).clone()
+            ar(xt, dst, beta=1)
+        torch.cuda.synchronize()
+        q.put((inputs.torch_to_bits(dst), fq.fault_flags()))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("n,kw", [((1 << 20) + 256 * 3 + 77, {}), (256 * 1000, {"scales": "e8m0"})])
+def test_nccl_single_rank_allreduce_matches_oracle(dev, n, kw):
+    """The NCCL path (payload slices staged on the device, NCCL all_to_all / all_gather) with the
+    one rank a single GPU allows: the result equals the oracle's reduce of the rank's payload
+    followed by its decode."""
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_nccl_worker, args=(_free_port(), n, kw, q))
+    p.start()
+    bits, flags = q.get(timeout=600)
+    p.join(timeout=120)
+    assert p.exitcode == 0
+    scales = kw.get("scales", "dual")
+    group = 32 if scales == "e8m0" else 16
+    x, d0 = _rank_inputs(n, 0)
+    pay = oracle.compress(x, group, 1, scales=scales)
+    want = oracle.decompress_accumulate(oracle.reduce_requantize([pay], n, group, scales=scales), n, d0.copy(), 1,
+                                        group, 1, scales=scales)
+    assert flags == 0
+    assert np.array_equal(bits, want)
