@@ -26,8 +26,9 @@
 // (InPipe: mbarrier-tracked cp.async.bulk.tensor loads with bounded waits), and BF16 / FP32
 // outputs leave by TMA stores from a swizzled staging buffer; where a tile needs one box per
 // block (strided rows that do not hold whole tiles) eight lanes issue them. Tiles are
-// assigned round robin to the warps of the grid; large reduces instead run one CTA per SM
-// whose warps claim tiles from a shared-memory counter. Every kernel starts with
+// assigned round robin to the warps of the grid; large tensors (compress and roundtrip of
+// BF16 input, decompress-accumulate into BF16 with beta = 1, the reduce) instead run one CTA
+// per SM whose warps claim the CTA's tiles from a shared-memory counter. Every kernel starts with
 // griddepcontrol.wait and is launched with programmatic stream serialisation, so
 // back-to-back codec kernels overlap launch and drain; for that overlap every kernel asks for
 // the largest shared-memory carveout, and a cap on CTAs per SM is enforced by padding the
