@@ -109,7 +109,7 @@ def sweep(n: int, seed: int = 0) -> np.ndarray:
 def edge_blocks() -> np.ndarray:
     """Hand-picked 256-element blocks that reach the contract's special cases: all zero,
     all -0, constant, one spike, tiny (subnormal-range) values, values near 2^119, exact
-    E4M3/E2M1 ties, alternating signs. Returned as bfloat16 bits, shape [k, 256]."""
+    E4M3/E2M1 ties, alternating signs, spikes at and just below the zero-block limit. Returned as bfloat16 bits, shape [k, 256]."""
     f = np.float32
     blocks = []
     blocks.append(np.zeros(256, f))
@@ -132,4 +132,10 @@ def edge_blocks() -> np.ndarray:
     b[64] = 1.78125
     b[80] = 2.0 ** -24; b[81] = -(2.0 ** -24)
     blocks.append(b)
+    # the zero-block limit A = 2688 * 2^-100 = 1.3125 * 2^-89 (a bfloat16 value): one spike at
+    # the limit and one a bfloat16 ulp below it, without the transform (A = |x|) and with it
+    # (a lone spike spreads to |x| / 16 on every element)
+    lim, below = 1.3125 * 2.0 ** -89, (1.3125 - 2.0 ** -7) * 2.0 ** -89
+    for v, at in ((lim, 9), (-below, 200), (-16 * lim, 77), (16 * below, 140)):
+        b = np.zeros(256, f); b[at] = v; blocks.append(b)
     return np.stack([to_bf16_bits(x) for x in blocks])

@@ -294,6 +294,28 @@ def test_all_zero_and_tiny_blocks_give_zero_payload():
     assert not oracle.compress(neg, group=16, fwht=1).any()
 
 
+@pytest.mark.parametrize("fwht", [0, 1])
+def test_zero_block_limit_is_inclusive_at_2688_times_2_pow_minus_100(fwht):
+    """A block whose maximum is exactly 2688 * 2^-100 is coded (s_b = 2^-100, the spike's
+    group scale 448 = 0x7E, its code 6 = 0x7); one bfloat16 ulp below, the block is all zero.
+    With the transform a lone spike x gives |y| = |x| / 16 everywhere, so the spike is 16x.
+    A mistaken comparison (<= instead of <) or a zero limit off by a factor fails here."""
+    k = 16.0 if fwht else 1.0
+    lim = 1.3125 * 2.0 ** -89
+    assert np.float32(2688.0) * np.float32(2.0 ** -100) == np.float32(lim)
+    at = np.zeros(256, np.float32); at[3] = k * lim
+    p = oracle.compress(inputs.to_bf16_bits(at), group=16, fwht=fwht)
+    codes, gsc, bsc = oracle.split_payload(p, 256, 16)
+    assert bsc[0] == np.float32(2.0 ** -100)
+    if fwht:      # every element is y = +-lim (row 3 of the Hadamard matrix): scales 448, codes +-6
+        assert np.all(gsc == 0x7E) and np.all(codes & 0x77 == 0x77)
+    else:
+        assert gsc[0] == 0x7E and not gsc[1:].any()
+        assert codes[1] == 0x70 and not np.delete(codes, 1).any()
+    below = np.zeros(256, np.float32); below[3] = -k * (1.3125 - 2.0 ** -7) * 2.0 ** -89
+    assert not oracle.compress(inputs.to_bf16_bits(below), group=16, fwht=fwht).any()
+
+
 # ---------------------------------------------------------------------------- whole codec
 
 def _decode_scales(p, n, G):
