@@ -9,6 +9,8 @@ import os
 import re
 import shutil
 
+import pytest
+
 import bench
 
 SRC = os.path.join(bench.ROOT, "fp4_communication_compression_gb300", "csrc")
@@ -138,3 +140,88 @@ def test_target_summary_counts_only_large_workloads():
     s = bench.target_summary(cfg)
     assert s["records"] == 2 and s["met"] == 1
     assert s["below"] == [{"big:roundtrip_g32_fwht0": 0.65}]
+    assert "back_to_back" not in s          # no record carries a back-to-back time
+
+
+def test_target_summary_counts_back_to_back_times_apart():
+    cfg = {"big": {"bytes_bf16": 1 << 26, "kernels": [
+        {"kernel": "compress", "frac_of_peak": 0.68, "stream_frac_of_peak": 0.74},
+        {"kernel": "reduce_r4", "frac_of_peak": 0.5, "stream_frac_of_peak": 0.59},
+        {"kernel": "compress", "frac_of_peak": 0.74, "stream_frac_of_peak": 0.74,
+         "variant": "compress_tc (fwht=2, relaxed parity)"}]}}
+    s = bench.target_summary(cfg)
+    assert s["records"] == 2 and s["met"] == 0
+    assert s["back_to_back"] == {"records": 2, "met": 1, "below": [{"big:reduce_r4": 0.59}], "min_frac": 0.59}
+
+
+def test_back_to_back_buffer_sets_cover_three_times_l2():
+    class Props:
+        L2_cache_size = 100
+
+    class FakeCuda:
+        @staticmethod
+        def get_device_properties(dev):
+            return Props()
+
+    class FakeTorch:
+        cuda = FakeCuda
+
+    t = bench.Timer.__new__(bench.Timer)
+    t.torch, t.dev = FakeTorch, None
+    assert t.buffer_sets(100) == 3 and t.buffer_sets(101) == 3 and t.buffer_sets(99) == 4
+    assert t.buffer_sets(1000) == 2          # never fewer than two sets
+    rec = bench.kernel_record("compress", 1 << 20, 1.0, 1000.0, stream_ms=0.5)
+    assert rec["stream_us"] == 500.0 and rec["stream_frac_of_peak"] == 2 * rec["frac_of_peak"]
+
+
+def test_back_to_back_hold_doubles_until_the_host_keeps_up():
+    """The start event must still be pending when the host has enqueued the region's last
+    launch; a region where it was not is taken again with twice the hold."""
+    log = []
+
+    class Event:
+        n = 0
+
+        def __init__(self, enable_timing=True):
+            pass
+
+        def record(self, stream):
+            pass
+
+        def query(self):              # passed already while the hold is below 2^24 cycles
+            return state["hold"] < (1 << 24)
+
+        def elapsed_time(self, other):
+            return 8.0
+
+    state = {"hold": 0}
+
+    class FakeCuda:
+        @staticmethod
+        def _sleep(cycles):
+            state["hold"] = cycles
+            log.append(cycles)
+
+        @staticmethod
+        def synchronize(dev=None):
+            pass
+
+    FakeCuda.Event = Event
+
+    class FakeTorch:
+        cuda = FakeCuda
+
+    t = bench.Timer.__new__(bench.Timer)
+    t.torch, t.dev, t.stream = FakeTorch, None, None
+    t.hold_cycles = 1 << 22
+    t.flush = lambda: None
+    calls = []
+    ms = t.stream_ms([lambda: calls.append(0)] * 2, reps=3, rounds=2)
+    assert ms == 2.0                              # 8 ms over 2 rounds x 2 launches
+    assert log == [1 << 22, 1 << 23, 1 << 24, 1 << 24, 1 << 24]
+    assert t.hold_cycles == 1 << 24
+    # a host that never keeps up ends in an error, not in a starved number
+    Event.query = lambda self: True
+    t.hold_cycles = 1 << 29
+    with pytest.raises(RuntimeError, match="longest hold"):
+        t.stream_ms([lambda: None], reps=1, rounds=1)
