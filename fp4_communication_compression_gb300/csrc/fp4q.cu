@@ -88,13 +88,15 @@ constexpr int64_t kReduceDynTilesPerWarpR2 = 8;
 // tiles claimed dynamically. The five CTAs of an SM were measured finishing up to 12 us apart
 // at 2^26 elements (the warps of one CTA within 1 us), the SM's last stretch running on few
 // warps; claimed dynamically they end within 2 us (compress 38.9 -> 37.4 us at 2^26, 69.6 ->
-// 67.7 at 2^27; roundtrip 61.4 -> 59.4, 113.5 -> 110.1). Below 8 tiles per warp it gained
-// nothing, and for the reduce below 384 tiles per SM it lost (R = 8 at 2^25: 47.2 -> 54.9 us).
+// 67.7 at 2^27; roundtrip 61.4 -> 59.4, 113.5 -> 110.1). From 4 tiles per warp (2^25
+// elements) it still gains a little: launched back to back, compress 0.650 -> 0.655 of the
+// copy peak, roundtrip 0.636 -> 0.643, decompress-accumulate (beta = 1) 0.86 -> 0.90. For the
+// reduce below 384 tiles per SM it lost (R = 8 at 2^25: 47.2 -> 54.9 us).
 constexpr int kCompressDynWarps = 20;
 // Decompress-accumulate into BF16 with beta = 1 likewise (its 4 CTAs x 4 warps as one CTA):
 // 48.2 -> 47.0 us at 2^26, 96.2 -> 95.7 us at 2^27, equal at 2^28 - 2^29.
 constexpr int kDecompressDynWarps = 16;
-constexpr int64_t kCompressDynTilesPerWarp = 8;
+constexpr int64_t kCompressDynTilesPerWarp = 4;
 constexpr int kDynHeaderBytes = 2048;      // barriers of up to 31 warps, the claim counter last
 constexpr float kZeroLimit = 2688.0f * 0x1p-100f;   // all-zero block guard on A_b
 constexpr unsigned kFull = 0xffffffffu;

@@ -1,8 +1,11 @@
-"""Parity of the dynamic-claim kernels on a ragged length: n = 2^26 + 3 * 256 + 77 elements is
+"""Parity of the dynamic-claim kernels on ragged lengths. n = 2^26 + 3 * 256 + 77 elements is
 above the size where compress, roundtrip, decompress-accumulate (BF16, beta = 1) and the
-R <= 2 reduce claim their tiles dynamically, its last tile holds three blocks and its last
-block is partial (zero-padded). The oracle checks a sample of blocks one by one (blocks are
-independent) that includes the first, the middle, the last full tile's and the tail blocks."""
+R <= 2 reduce claim their tiles dynamically; n = 12160 * 2048 + 5 * 256 + 33 is one ragged
+tile above the smallest size where compress, roundtrip and decompress-accumulate do (4 tiles
+of 2048 elements per warp, 20 (compress) or 16 (decompress) warps per SM, 152 SMs). In both
+the last tile is partial and the last block is partial (zero-padded). The oracle checks a
+sample of blocks one by one (blocks are independent) that includes the first, the middle, the
+last full tile's and the tail blocks."""
 import numpy as np
 import pytest
 import torch
@@ -12,9 +15,7 @@ import fp4_communication_compression_gb300 as fq
 from fp4_communication_compression_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
-N = (1 << 26) + 3 * 256 + 77
-M = (N + 255) // 256 * 256          # the payload's (padded) length
-NB = M // 256
+SIZES = [(1 << 26) + 3 * 256 + 77, 12160 * 2048 + 5 * 256 + 33]
 
 
 @pytest.fixture(scope="module")
@@ -25,14 +26,28 @@ def dev():
     return torch.device("cuda:0")
 
 
+class Case:
+    def __init__(self, n):
+        self.N = n
+        self.M = (n + 255) // 256 * 256      # the payload's (padded) length
+        self.NB = self.M // 256
+
+
+@pytest.fixture(scope="module", params=SIZES, ids=["2p26_ragged", "threshold_ragged"])
+def case(request):
+    return Case(request.param)
+
+
 @pytest.fixture(scope="module")
-def blocks():
+def blocks(case):
+    NB = case.NB
     rng = np.random.default_rng(2609)
     fixed = [0, 1, 7, 8, NB // 2, NB - 12, NB - 9, NB - 5, NB - 4, NB - 3, NB - 2, NB - 1]
     return np.unique(np.concatenate([fixed, rng.choice(NB, 400, replace=False)]))
 
 
-def make_x(seed):
+def make_x(case, seed):
+    N, NB = case.N, case.NB
     rng = np.random.default_rng(seed)
     v = rng.standard_normal(N, dtype=np.float32)
     v *= np.exp(rng.uniform(-2, 2, NB).astype(np.float32)).repeat(256)[:N]
@@ -40,25 +55,26 @@ def make_x(seed):
 
 
 @pytest.fixture(scope="module")
-def xs(dev):
-    return [make_x(s) for s in (261, 262)]
+def xs(dev, case):
+    return [make_x(case, s) for s in (261, 262)]
 
 
-def sample_elems(bits, blocks):
+def sample_elems(case, bits, blocks):
     """The sampled blocks' elements, zero-padded past n (the payload's own padding)."""
     out = np.zeros((blocks.size, 256), bits.dtype)
     for i, b in enumerate(blocks):
-        seg = bits[b * 256:min((b + 1) * 256, N)]
+        seg = bits[b * 256:min((b + 1) * 256, case.N)]
         out[i, :seg.size] = seg
     return out.ravel()
 
 
-def valid_mask(blocks):
-    return ((blocks[:, None] * 256 + np.arange(256)[None, :]) < N).ravel()
+def valid_mask(case, blocks):
+    return ((blocks[:, None] * 256 + np.arange(256)[None, :]) < case.N).ravel()
 
 
-def gather(payload, blocks, G=16):
+def gather(case, payload, blocks, G=16):
     """The sampled blocks' segments as the payload of len(blocks) * 256 elements."""
+    M, NB = case.M, case.NB
     p = payload.cpu().numpy()
     gs = 256 // G
     codes = p[:M // 2].reshape(NB, 128)[blocks].ravel()
@@ -75,35 +91,35 @@ def gather(payload, blocks, G=16):
     return out
 
 
-def test_compress_and_decompress_accumulate(dev, xs, blocks):
+def test_compress_and_decompress_accumulate(dev, case, xs, blocks):
     xb = xs[0]
     p = fq.compress(inputs.bits_to_torch(xb, dev))
-    want = oracle.compress(sample_elems(xb, blocks))
-    assert np.array_equal(gather(p, blocks), want)
+    want = oracle.compress(sample_elems(case, xb, blocks))
+    assert np.array_equal(gather(case, p, blocks), want)
     # beta = 1 into a BF16 residual
-    resid = make_x(263)
+    resid = make_x(case, 263)
     d = inputs.bits_to_torch(resid, dev).clone()
-    fq.decompress_accumulate(p, N, d, beta=1)
+    fq.decompress_accumulate(p, case.N, d, beta=1)
     got = inputs.torch_to_bits(d)
-    ref = oracle.decompress_accumulate(want, blocks.size * 256, sample_elems(resid, blocks), beta=1)
-    keep = valid_mask(blocks)
-    assert np.array_equal(sample_elems(got, blocks)[keep], ref[keep])
+    ref = oracle.decompress_accumulate(want, blocks.size * 256, sample_elems(case, resid, blocks), beta=1)
+    keep = valid_mask(case, blocks)
+    assert np.array_equal(sample_elems(case, got, blocks)[keep], ref[keep])
     assert fq.fault_flags() == 0
 
 
-def test_roundtrip(dev, xs, blocks):
+def test_roundtrip(dev, case, xs, blocks):
     xb = xs[1]
     y = fq.roundtrip(inputs.bits_to_torch(xb, dev))
-    got = sample_elems(inputs.torch_to_bits(y), blocks)
-    ref = oracle.roundtrip(sample_elems(xb, blocks))
-    keep = valid_mask(blocks)
+    got = sample_elems(case, inputs.torch_to_bits(y), blocks)
+    ref = oracle.roundtrip(sample_elems(case, xb, blocks))
+    keep = valid_mask(case, blocks)
     assert np.array_equal(got[keep], ref[keep])
     assert fq.fault_flags() == 0
 
 
-def test_two_rank_reduce(dev, xs, blocks):
+def test_two_rank_reduce(dev, case, xs, blocks):
     pays = [fq.compress(inputs.bits_to_torch(x, dev)) for x in xs]
-    red = fq.reduce_requantize(pays, N)
-    want = oracle.reduce_requantize([gather(p, blocks) for p in pays], blocks.size * 256)
-    assert np.array_equal(gather(red, blocks), want)
+    red = fq.reduce_requantize(pays, case.N)
+    want = oracle.reduce_requantize([gather(case, p, blocks) for p in pays], blocks.size * 256)
+    assert np.array_equal(gather(case, red, blocks), want)
     assert fq.fault_flags() == 0
