@@ -764,6 +764,12 @@ __device__ __forceinline__ void pay_scales(const PayRaw& r, int l4, float S[4]) 
 // next kernel's CTAs be scheduled as soon as SM resources free up.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Fetch a tensor map's descriptor before the first copy that uses it. A kernel parameter is
+// not written by an earlier kernel, so this may run before grid_dependency_wait: under
+// programmatic serialisation the fetch then overlaps the previous kernel's tail.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
 
 // Shared-memory primitives (sm_90+ PTX: mbarrier, cp.async.bulk.tensor, proxy fences).
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -1245,6 +1251,7 @@ __global__ void __launch_bounds__(DYN ? kCompressDynWarps * 32 : kCompressWarps 
 compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T) {
   constexpr int IN = XF ? 8192 : 4096;
   extern __shared__ uint8_t smem_raw[];
+  if (threadIdx.x == 0) prefetch_tensormap(&xmap);
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
@@ -1303,6 +1310,7 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
   constexpr int LPB = DT == FP4Q_BF16 ? 4 : 8;   // 128-byte lines per block of dst
   constexpr bool LB = FWHT != 0;
   extern __shared__ uint8_t smem_raw[];
+  if (threadIdx.x == 0) prefetch_tensormap(&dmap);
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
@@ -1381,6 +1389,8 @@ __global__ void __launch_bounds__(DYN ? kCompressDynWarps * 32 : kRoundtripWarps
 roundtrip_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap, TileLoop T) {
   constexpr int IN = XF ? 8192 : 4096;
   extern __shared__ uint8_t smem_raw[];
+  if (threadIdx.x == 0) prefetch_tensormap(&xmap);
+  if (threadIdx.x == 32) prefetch_tensormap(&ymap);
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, blk = lane >> 2, l4 = lane & 3;
