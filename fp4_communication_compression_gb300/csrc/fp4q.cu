@@ -918,11 +918,15 @@ __device__ __forceinline__ WarpSmem warp_smem(uint8_t* raw, int warp) {
 // Tiles come round robin (warp w of W takes w, w + W, ...), or with DYN from the CTA's
 // claim counter in shared memory: CTA c's tiles are c, c + G, c + 2G, ... (G = gridDim.x)
 // and its warps take them in the order they ask, so warps that run ahead do more tiles.
+// With `defer` the start loads only the first stage and the first refill the others, so
+// that every warp's first tile reaches the head of the memory queue (the 3- and 4-rank
+// reduce: 0.554 -> 0.581 of the copy peak at 2^25 back to back, 0.603 -> 0.617 at 2^26;
+// no gain for the other kernels, a small loss for 2 ranks).
 template <int STAGES, int BYTES, bool ALL_LANES = false, bool DYN = false>
 struct InPipe {
   uint32_t stage0, bar0;
   int64_t t0, W, tiles;
-  int i, issued;
+  int i, issued, deferred;      // iterations whose copies were issued, stages the start left out
   uint32_t ctr, asked;          // DYN: the CTA's counter (shared address), lane 0's claim
   int64_t tid[DYN ? STAGES : 1];  // DYN: the tile each stage holds
 
@@ -940,7 +944,7 @@ struct InPipe {
 
   template <class Issue>
   __device__ __forceinline__ void start(uint32_t stage0_, uint32_t bar0_, int64_t t0_, int64_t W_,
-                                        int64_t tiles_, int lane, Issue&& issue) {
+                                        int64_t tiles_, int lane, Issue&& issue, bool defer = false) {
     stage0 = stage0_;
     bar0 = bar0_;
     t0 = t0_;
@@ -952,7 +956,8 @@ struct InPipe {
     }
     __syncwarp();
     issued = 0;
-    for (int s = 0; s < STAGES; ++s) {
+    deferred = defer ? STAGES - 1 : 0;
+    for (int s = 0; s < STAGES - deferred; ++s) {
       const int64_t t = t0 + (int64_t)s * W;
       if (t < tiles) {
         if (ALL_LANES || lane == 0) issue(buf(s), bar(s), t);
@@ -965,7 +970,7 @@ struct InPipe {
   // dyn_counter_init before any warp gets here).
   template <class Issue>
   __device__ __forceinline__ void start_dyn(uint32_t stage0_, uint32_t bar0_, uint32_t ctr_, int64_t tiles_, int lane,
-                                            Issue&& issue) {
+                                            Issue&& issue, bool defer = false) {
     static_assert(DYN, "start_dyn needs DYN");
     stage0 = stage0_;
     bar0 = bar0_;
@@ -977,9 +982,10 @@ struct InPipe {
     }
     __syncwarp();
     issued = 0;
+    deferred = defer ? STAGES - 1 : 0;
     for (int s = 0; s < STAGES; ++s) {
       tid[s] = claim_tile(claim_ask(lane));
-      if (tid[s] < tiles) {
+      if (s < STAGES - deferred && tid[s] < tiles) {
         if (ALL_LANES || lane == 0) issue(buf(s), bar(s), tid[s]);
         ++issued;
       }
@@ -1021,6 +1027,16 @@ struct InPipe {
   __device__ __forceinline__ void refill(int lane, Issue&& issue) {
     fence_proxy_async();
     __syncwarp();
+    if (deferred) {
+      for (int s = STAGES - deferred; s < STAGES; ++s) {
+        const int64_t t = DYN ? tid[s] : t0 + (int64_t)s * W;
+        if (t < tiles) {
+          if (ALL_LANES || lane == 0) issue(buf(s), bar(s), t);
+          ++issued;
+        }
+      }
+      deferred = 0;
+    }
     const int64_t tn = DYN ? claim_tile(asked) : t0 + (int64_t)(i + STAGES) * W;
     if (DYN) tid[i % STAGES] = tn;
     if (tn < tiles) {
@@ -1549,13 +1565,14 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
     }
   };
   InPipe<C::kStagesR, C::kStageBytes, true, DYN> pipe{};
+  // the direct-scale variants (R = 3, 4) defer all but their first stage (see InPipe)
   if constexpr (DYN) {
     const uint32_t ctr = ((smem_addr(smem_raw) + 127u) & ~127u) + (uint32_t)(C::kDynWarps * C::kRegion);
     dyn_counter_init(ctr);
-    pipe.start_dyn(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), ctr, T.tiles, lane, issue);
+    pipe.start_dyn(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), ctr, T.tiles, lane, issue, DS);
   } else {
     pipe.start(base, base + (uint32_t)(C::kStagesR * C::kStageBytes), warp_global<kReduceWarps>(),
-               warp_count<kReduceWarps>(), T.tiles, lane, issue);
+               warp_count<kReduceWarps>(), T.tiles, lane, issue, DS);
   }
   if (DS) load_scales(DYN ? pipe.tile() : pipe.t0, cg, cs);
   for (int64_t t = DYN ? pipe.tile() : pipe.t0; t < T.tiles; t = DYN ? pipe.tile() : t + pipe.W) {
