@@ -260,10 +260,11 @@ def test_back_to_back_chain_keeps_stream_order(dev):
 @pytest.mark.parametrize("nb", [1, 2, 3, 4, 5, 6, 7, 9, 13, 8 * 97 + 3, 8 * 2431 + 7])
 def test_reduce_ragged_tails(dev, nb, G):
     """Block counts with every remainder modulo the 8-block tile: the last tile's codes,
-    group scales and block scales are partly bulk-copied and partly loaded directly."""
+    group scales and block scales are partly bulk-copied and partly loaded directly. R = 3, 4
+    also cover the deferred pipeline start on warps with one tile or none."""
     n = 256 * nb
-    xs = [inputs.sweep(n, seed=s).ravel() for s in (5, 6, 7)]
-    for R in (1, 2, 3):
+    xs = [inputs.sweep(n, seed=s).ravel() for s in (5, 6, 7, 8)]
+    for R in (1, 2, 3, 4):
         pays = [fq.compress(inputs.bits_to_torch(x, dev), group=G) for x in xs[:R]]
         refs = [oracle.compress(x, group=G) for x in xs[:R]]
         torch.cuda.synchronize()
