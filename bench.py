@@ -451,7 +451,7 @@ def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
         """Back-to-back time per launch (Timer.stream_ms) over buffer sets of `footprint`
         bytes, each make() a launch on a fresh set; only for the workloads the 70% target
         applies to (None below that size)."""
-        if 2 * n < TARGET_MIN_BYTES:
+        if 2 * n < TARGET_MIN_BYTES or not hasattr(torch.cuda, "_sleep"):   # no spin kernel: no hold
             return None
         fns = [make() for _ in range(timer.buffer_sets(footprint))]
         try:
