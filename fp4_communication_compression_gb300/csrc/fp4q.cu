@@ -93,8 +93,10 @@ constexpr int64_t kReduceDynTilesPerWarpR2 = 8;
 // copy peak, roundtrip 0.636 -> 0.643, decompress-accumulate (beta = 1) 0.86 -> 0.90. For the
 // reduce below 384 tiles per SM it lost (R = 8 at 2^25: 47.2 -> 54.9 us).
 constexpr int kCompressDynWarps = 20;
-// Decompress-accumulate into BF16 with beta = 1 likewise (its 4 CTAs x 4 warps as one CTA):
-// 48.2 -> 47.0 us at 2^26, 96.2 -> 95.7 us at 2^27, equal at 2^28 - 2^29.
+// Decompress-accumulate into BF16 likewise (its 4 CTAs x 4 warps as one CTA). beta = 1:
+// 48.2 -> 47.0 us at 2^26, 96.2 -> 95.7 us at 2^27, equal at 2^28 - 2^29. beta = 0 (no
+// destination pipeline; the warps claim from the counter directly): 0.72 -> 0.73 of the copy
+// peak at 2^26, 0.78 -> 0.81 at 2^27, 0.86 -> 0.89 at 2^29, within the timer's step at 2^25.
 constexpr int kDecompressDynWarps = 16;
 constexpr int64_t kCompressDynTilesPerWarp = 4;
 constexpr int kDynHeaderBytes = 2048;      // barriers of up to 31 warps, the claim counter last
@@ -1233,6 +1235,13 @@ __device__ __forceinline__ void dyn_counter_init(uint32_t ctr) {
   if (threadIdx.x == 0) asm volatile("st.shared.u32 [%0], 0;" ::"r"(ctr) : "memory");
   __syncthreads();
 }
+// One tile claimed from a CTA's counter by a warp with no load pipeline (InPipe DYN claims
+// the same way): CTA c's tiles are c, c + G, c + 2G, ... (G = gridDim.x); every lane gets it.
+__device__ __forceinline__ int64_t claim_plain(uint32_t ctr, int lane) {
+  uint32_t c = 0;
+  if (lane == 0) asm volatile("atom.shared.add.u32 %0, [%1], 1;" : "=r"(c) : "r"(ctr) : "memory");
+  return (int64_t)blockIdx.x + (int64_t)__shfl_sync(kFull, c, 0) * gridDim.x;
+}
 
 template <int WARPS>
 __device__ __forceinline__ int64_t warp_global() {
@@ -1321,7 +1330,7 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
 template <int G, int FWHT, int DT, int BETA, bool MX, bool DYN = false>
 __global__ void __launch_bounds__(DYN ? kDecompressDynWarps * 32 : kDecompressWarps * 32, DYN ? 1 : kDecompressCtas)
 decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop T) {
-  static_assert(!DYN || (BETA && DT == FP4Q_BF16), "dynamic claims ride on the destination pipeline");
+  static_assert(!DYN || DT == FP4Q_BF16, "dynamic claims: BF16 destinations");
   constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
   constexpr int LPB = DT == FP4Q_BF16 ? 4 : 8;   // 128-byte lines per block of dst
   constexpr bool LB = FWHT != 0;
@@ -1333,13 +1342,18 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
   const WarpSmem ws = warp_smem<kDecompressStages, BETA ? TB : 0, kXBufBytes, DYN ? kDynHeaderBytes : kHeaderBytes>(smem_raw, warp);
   const XposeAddr xa = xpose_addr(ws.xbuf, blk, l4);
   auto issue = [&](uint32_t buf, uint32_t bar, int64_t t) { tile_load<LPB>(&dmap, T, t, buf, bar, lane); };
-  InPipe<kDecompressStages, TB, true, DYN> pipe{};
+  InPipe<kDecompressStages, TB, true, DYN && BETA> pipe{};
   int64_t t0, W;
+  uint32_t ctr = 0;
   if constexpr (DYN) {
-    const uint32_t ctr = dyn_counter_addr(smem_raw);
+    ctr = dyn_counter_addr(smem_raw);
     dyn_counter_init(ctr);
-    pipe.start_dyn(ws.stage0, ws.bar0, ctr, T.tiles, lane, issue);
-    t0 = pipe.tile();
+    if constexpr (BETA) {
+      pipe.start_dyn(ws.stage0, ws.bar0, ctr, T.tiles, lane, issue);
+      t0 = pipe.tile();
+    } else {
+      t0 = claim_plain(ctr, lane);    // no destination pipeline: the counter directly
+    }
     W = 0;
   } else {
     t0 = warp_global<kDecompressWarps>();
@@ -1349,11 +1363,13 @@ decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop 
   PayRaw cur, nxt;
   if (t0 < T.tiles && t0 * kTileBlocks + blk < T.nb) pay_load<G, LB, MX>(P, t0 * kTileBlocks + blk, l4, cur);
   else pay_zero(cur);
-  for (int64_t t = t0; t < T.tiles; t = DYN ? pipe.tile() : t + W) {
-    int64_t tn;
-    if constexpr (DYN) {
+  int64_t tn = 0;
+  for (int64_t t = t0; t < T.tiles; t = DYN ? (BETA ? pipe.tile() : tn) : t + W) {
+    if constexpr (DYN && BETA) {
       pipe.ask(lane);
       tn = pipe.asked_tile();
+    } else if constexpr (DYN) {
+      tn = claim_plain(ctr, lane);
     } else {
       tn = t + W;
     }
@@ -2069,13 +2085,13 @@ fp4q_status launch_decompress(const Payload& P, int64_t n, void* dst, cudaStream
     const int sms = num_sms();
     fp4q_status st = FP4Q_OK;
     bool dyn = false;
-    if constexpr (DT == FP4Q_BF16 && B == 1) {
+    if constexpr (DT == FP4Q_BF16) {
       dyn = sms > 0 && T.tiles >= kCompressDynTilesPerWarp * kDecompressDynWarps * sms;
       if (dyn) {
         auto k = decompress_kernel<G, F, DT, B, MX, true>;
         Launch L;
         st = plan(k, kDecompressDynWarps,
-                  WarpSmemLayout<kDecompressDynWarps, kDecompressStages, TB, kXBufBytes, kDynHeaderBytes>::kCtaBytes,
+                  WarpSmemLayout<kDecompressDynWarps, kDecompressStages, B ? TB : 0, kXBufBytes, kDynHeaderBytes>::kCtaBytes,
                   T.tiles, L, 1);
         if (st == FP4Q_OK) st = launch_pdl(k, L, kDecompressDynWarps * 32, s, dm, P, T);
       }

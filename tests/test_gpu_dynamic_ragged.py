@@ -1,5 +1,5 @@
 """Parity of the dynamic-claim kernels on ragged lengths. n = 2^26 + 3 * 256 + 77 elements is
-above the size where compress, roundtrip, decompress-accumulate (BF16, beta = 1) and the
+above the size where compress, roundtrip, decompress-accumulate (BF16, beta = 0 and 1) and the
 R <= 2 reduce claim their tiles dynamically; n = 12160 * 2048 + 5 * 256 + 33 is one ragged
 tile above the smallest size where compress, roundtrip and decompress-accumulate do (4 tiles
 of 2048 elements per warp, 20 (compress) or 16 (decompress) warps per SM, 152 SMs). In both
@@ -104,6 +104,11 @@ def test_compress_and_decompress_accumulate(dev, case, xs, blocks):
     ref = oracle.decompress_accumulate(want, blocks.size * 256, sample_elems(case, resid, blocks), beta=1)
     keep = valid_mask(case, blocks)
     assert np.array_equal(sample_elems(case, got, blocks)[keep], ref[keep])
+    # beta = 0 (the decode alone) into a BF16 buffer
+    d0 = torch.full_like(d, 3.0)
+    fq.decompress_accumulate(p, case.N, d0, beta=0)
+    ref0 = oracle.decompress_accumulate(want, blocks.size * 256, np.zeros(blocks.size * 256, np.uint16), beta=0)
+    assert np.array_equal(sample_elems(case, inputs.torch_to_bits(d0), blocks)[keep], ref0[keep])
     assert fq.fault_flags() == 0
 
 
