@@ -1517,7 +1517,8 @@ struct ReduceCfg {
   // launch bound (CTAs per SM): 5 where the kernel fits 96 registers without spilling its
   // running sum (R = 2: 21.6 -> 20.5 us, R = 8: 49.2 -> 47.1 us at 2^25 elements); the R = 3, 4
   // variants prefetch every rank's scales into registers and keep 4 (at 5 they spill: R = 4
-  // went from 29.4 to 36.8 us)
+  // went from 29.4 to 36.8 us); R = 2 at 6 (80 registers, spilling) lost at every size (0.48 ->
+  // 0.41 of the copy peak back to back at 2^25)
   static constexpr int kMinCtas = (R == 3 || R == 4) ? 4 : 5;
   // dynamic-claim CTAs (InPipe DYN) hold as many warps as that fixed grid has per SM
   static constexpr int kDynWarps = 4 * kMinCtas;
