@@ -77,8 +77,10 @@ def test_large_compress_decompress_roundtrip(dev, x, blocks, scales, G, fwht):
     assert fq.fault_flags() == 0
 
 
-@pytest.mark.parametrize("R", [2, 3, 8])
+@pytest.mark.parametrize("R", [2, 3, 4, 8])
 def test_large_reduce(dev, x, blocks, R):
+    """At 2^27 elements R = 2 and R >= 3 run their dynamic-claim CTAs (R = 3, 4 with the
+    deferred pipeline start and the prefetched scales, R = 8 without)."""
     xb, xt = x
     idx = block_elems(blocks)
     pays = [fq.compress(xt * (1.0 + 0.25 * r)) for r in range(R)]
