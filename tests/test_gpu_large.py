@@ -72,6 +72,14 @@ def test_large_compress_decompress_roundtrip(dev, x, blocks, scales, G, fwht):
     fq.decompress_accumulate(p, N, d, beta=1, **kw)
     ref = oracle.decompress_accumulate(want, idx.size, np.ones(idx.size, np.float32), beta=1, **kw)
     assert np.array_equal(d[torch.from_numpy(idx).to(dev)].cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    del d
+    # BF16 destinations (the dynamic-claim decode at this size), beta = 0 and 1 onto 0.5
+    for beta in (0, 1):
+        d16 = torch.full((N,), 0.5, dtype=torch.bfloat16, device=dev)
+        fq.decompress_accumulate(p, N, d16, beta=beta, **kw)
+        ref16 = oracle.decompress_accumulate(want, idx.size, np.full(idx.size, 0x3F00, np.uint16), beta=beta, **kw)
+        assert np.array_equal(inputs.torch_to_bits(d16[torch.from_numpy(idx).to(dev)]), ref16)
+        del d16
     y = fq.roundtrip(xt, **kw)
     assert np.array_equal(inputs.torch_to_bits(y[torch.from_numpy(idx).to(dev)]), oracle.roundtrip(xb[idx], **kw))
     assert fq.fault_flags() == 0
