@@ -484,16 +484,17 @@ def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
         return rec
 
     def codec_records(x_bits, tag, group=16, fwht=1, kernels=("compress", "decompress_bf16_b0",
-                                                              "decompress_bf16_b1", "roundtrip"), tc=False):
+                                                              "decompress_bf16_b1", "roundtrip"), tc=False,
+                      scales="dual"):
         """compress / decompress / roundtrip of one tensor: timings, parity, rel L2."""
         x_bits = np.ascontiguousarray(x_bits).ravel()
         n = x_bits.size
-        kw = dict(group=group, fwht=fwht)
+        kw = dict(group=group, fwht=fwht, scales=scales)
         x = to_dev(x_bits)
         pay = fq.compress(x, **kw)
-        want = oracle.compress(x_bits, group, fwht)
+        want = oracle.compress(x_bits, group, fwht, scales=scales)
         got = pay.cpu().numpy()
-        cmis, smis = payload_mismatch(got, want, n, group)
+        cmis, smis = payload_mismatch(got, want, n, group, scales)
         recs = []
         dst0 = residual(n, 1000 + n % 997)
         dst = dst0.clone()
@@ -503,7 +504,7 @@ def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
                 ms = timer.mean_ms(lambda: fq.compress(x, payload=pay, **kw), iters)
                 sms = b2b(n, 2 * n + pay.numel(), lambda: (lambda xc=x.clone(), pc=torch.empty_like(pay):
                                                              fq.compress(xc, payload=pc, **kw)))
-                recs.append(kernel_record(k, n, ms, peak, group, stream_ms=sms, code_mismatches=cmis,
+                recs.append(kernel_record(k, n, ms, peak, group, scales, stream_ms=sms, code_mismatches=cmis,
                                           scale_byte_mismatches=smis))
             elif k.startswith("decompress"):
                 beta = int(k[-1])
@@ -513,21 +514,25 @@ def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
                 dst.copy_(dst0)
                 fq.decompress_accumulate(pay, n, dst, beta=beta, **kw)
                 d0 = inputs.torch_to_bits(dst0)
-                ref = oracle.decompress_accumulate(got, n, d0, beta=beta, group=group, fwht=fwht)
+                ref = oracle.decompress_accumulate(got, n, d0, beta=beta, group=group, fwht=fwht, scales=scales)
                 vm = int(np.count_nonzero(inputs.torch_to_bits(dst) != ref))
-                recs.append(kernel_record(k, n, ms, peak, group, stream_ms=sms, value_mismatches=vm))
+                recs.append(kernel_record(k, n, ms, peak, group, scales, stream_ms=sms, value_mismatches=vm))
             elif k == "roundtrip":
                 ms = timer.mean_ms(lambda: fq.roundtrip(x, y=y, **kw), iters)
                 sms = b2b(n, 4 * n, lambda: (lambda xc=x.clone(), yc=torch.empty_like(y): fq.roundtrip(xc, y=yc, **kw)))
                 # roundtrip = decode(compress(x)) with beta = 0: against the oracle's decode of
                 # its own payload
-                ref = oracle.decompress_accumulate(want, n, np.zeros(n, np.uint16), beta=0, group=group, fwht=fwht)
+                ref = oracle.decompress_accumulate(want, n, np.zeros(n, np.uint16), beta=0, group=group, fwht=fwht,
+                                                   scales=scales)
                 vm = int(np.count_nonzero(inputs.torch_to_bits(y) != ref))
-                recs.append(kernel_record(k, n, ms, peak, group, stream_ms=sms, value_mismatches=vm))
+                recs.append(kernel_record(k, n, ms, peak, group, scales, stream_ms=sms, value_mismatches=vm))
         fq.roundtrip(x, y=y, **kw)
         err = rel_l2(torch, y.float(), x.float())
         del pay, dst, dst0, y
-        if tc and fwht == 1:
+        if scales != "dual":
+            for r in recs:
+                r["variant"] = f"{scales} (microscaled scales)"
+        if tc and fwht == 1 and scales == "dual":
             recs.append(tc_record(x, x_bits, n, group, want))
         del x
         return recs, err
@@ -618,13 +623,23 @@ def run_configs(torch, dev, fq, inputs, timer, peak, iters, headline_x=None):
         out[f"C5_sweep_2p{n.bit_length() - 1}"] = {"n": n, "bytes_bf16": 2 * n, "kernels": recs,
                                                   "rel_l2_error": {"roundtrip": round(err, 6)}}
         torch.cuda.empty_cache()
+
+    # the microscaled variant: E8M0 scales per group of 32, no block scale, on the size-sweep
+    # tensor (listed apart from the 70% target, which is stated for the dual-scale codec)
+    for n in (1 << 25, 1 << 27):
+        recs, err = codec_records(inputs.sweep(n), "sweep", group=32, fwht=1, scales="e8m0",
+                                  kernels=("compress", "decompress_bf16_b0", "decompress_bf16_b1", "roundtrip"))
+        out[f"F2_e8m0_sweep_2p{n.bit_length() - 1}"] = {"n": n, "bytes_bf16": 2 * n, "scales": "e8m0", "group": 32,
+                                                         "kernels": recs, "rel_l2_error": {"roundtrip": round(err, 6)}}
+        torch.cuda.empty_cache()
     return out
 
 
 def target_summary(configs):
     """Every bit-exact kernel record of a workload of at least 64 MiB of BF16 against the 70%
-    target (the relaxed tensor-core encoder is listed apart, in "tensor_core_encoder")."""
-    rows, below, tc = [], [], []
+    target. The relaxed tensor-core encoder ("tensor_core_encoder") and the microscaled E8M0
+    variant ("e8m0_variant": single-launch and back-to-back fractions) are listed apart."""
+    rows, below, tc, mx = [], [], [], []
     srows, sbelow = [], []
     for name, c in configs.items():
         if c["bytes_bf16"] < TARGET_MIN_BYTES:
@@ -632,6 +647,9 @@ def target_summary(configs):
         for k in c["kernels"]:
             if "relaxed" in k.get("variant", ""):
                 tc.append({f"{name}:compress_tc" + (f"_g{k['group']}" if "group" in k else ""): k["frac_of_peak"]})
+                continue
+            if "microscaled" in k.get("variant", ""):
+                mx.append({f"{name}:{k['kernel']}": [k["frac_of_peak"], k.get("stream_frac_of_peak")]})
                 continue
             tag = f"{name}:{k['kernel']}" + (f"_g{k['group']}_fwht{k['fwht']}" if "group" in k else "")
             rows.append(k["frac_of_peak"])
@@ -642,7 +660,7 @@ def target_summary(configs):
                 if k["stream_frac_of_peak"] < TARGET_FRAC:
                     sbelow.append({tag: k["stream_frac_of_peak"]})
     out = {"target_frac": TARGET_FRAC, "records": len(rows), "met": len(rows) - len(below), "below": below,
-           "min_frac": min(rows) if rows else None, "tensor_core_encoder": tc}
+           "min_frac": min(rows) if rows else None, "tensor_core_encoder": tc, "e8m0_variant": mx}
     if srows:
         out["back_to_back"] = {"records": len(srows), "met": len(srows) - len(sbelow), "below": sbelow,
                                "min_frac": min(srows)}

@@ -225,3 +225,15 @@ def test_back_to_back_hold_doubles_until_the_host_keeps_up():
     t.hold_cycles = 1 << 29
     with pytest.raises(RuntimeError, match="longest hold"):
         t.stream_ms([lambda: None], reps=1, rounds=1)
+
+
+def test_target_summary_lists_the_e8m0_variant_apart():
+    cfg = {"F2": {"bytes_bf16": 1 << 27, "kernels": [
+        {"kernel": "compress", "frac_of_peak": 0.6, "stream_frac_of_peak": 0.7,
+         "variant": "e8m0 (microscaled scales)"}]},
+           "C5": {"bytes_bf16": 1 << 27, "kernels": [{"kernel": "compress", "frac_of_peak": 0.8}]}}
+    s = bench.target_summary(cfg)
+    assert s["records"] == 1 and s["met"] == 1
+    assert s["e8m0_variant"] == [{"F2:compress": [0.6, 0.7]}]
+    rec = bench.kernel_record("compress", 1 << 20, 1.0, 1000.0, 32, "e8m0")
+    assert rec["alg_bytes_per_elem"] == 2.53125
