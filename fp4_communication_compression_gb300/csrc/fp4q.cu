@@ -922,8 +922,9 @@ __device__ __forceinline__ WarpSmem warp_smem(uint8_t* raw, int warp) {
 // and its warps take them in the order they ask, so warps that run ahead do more tiles.
 // With `defer` the start loads only the first stage and the first refill the others, so
 // that every warp's first tile reaches the head of the memory queue (the 3- and 4-rank
-// reduce: 0.554 -> 0.581 of the copy peak at 2^25 back to back, 0.603 -> 0.617 at 2^26;
-// no gain for the other kernels, a small loss for 2 ranks).
+// reduce: 0.554 -> 0.581 of the copy peak at 2^25 back to back, 0.603 -> 0.617 at 2^26; the
+// 2-rank reduce gains with it once it also reads its scales directly; no gain for the
+// other kernels).
 template <int STAGES, int BYTES, bool ALL_LANES = false, bool DYN = false>
 struct InPipe {
   uint32_t stage0, bar0;
@@ -1507,15 +1508,17 @@ constexpr bool kReduceDirectScales = true;
 
 template <int R>
 struct ReduceCfg {
-  // R = 3, 4 (dual scales): the scales are read straight from global memory one tile ahead,
-  // so the bulk copies carry only the codes (at 2^28 elements R = 4 gains 5%). For R = 2 the
-  // extra load latency costs more than the two copies per rank save at small sizes, the
-  // E8M0 scales are only 2 bytes per lane, and above R = 4 the prefetch needs too many
-  // registers.
-  static constexpr bool kDirectScales = kReduceDirectScales && R >= 3 && R <= 4;
+  // R = 2 - 4 (dual scales): the scales are read straight from global memory one tile ahead,
+  // so the bulk copies carry only the codes (at 2^28 elements R = 4 gains 5%). R = 2 gains
+  // since the pipeline start was deferred (0.48 -> 0.52 of the copy peak back to back at 2^25,
+  // 0.57 -> 0.61 at 2^26, 0.61 -> 0.66 at 2^27); before, the extra load latency cost more
+  // than the two copies per rank saved. The E8M0 scales are only 2 bytes per lane, and above
+  // R = 4 the single stage leaves no next tile to prefetch for.
+  static constexpr bool kDirectScales = kReduceDirectScales && R >= 2 && R <= 4;
   static constexpr int kStagesR = R <= 4 ? 2 : 1;
   // launch bound (CTAs per SM): 5 where the kernel fits 96 registers without spilling its
-  // running sum (R = 2: 21.6 -> 20.5 us, R = 8: 49.2 -> 47.1 us at 2^25 elements); the R = 3, 4
+  // running sum (R = 2: 21.6 -> 20.5 us, R = 8: 49.2 -> 47.1 us at 2^25 elements; R = 2 with
+  // the direct scales spills 8 bytes at G = 16 and is faster all the same); the R = 3, 4
   // variants prefetch every rank's scales into registers and keep 4 (at 5 they spill: R = 4
   // went from 29.4 to 36.8 us); R = 2 at 6 (80 registers, spilling) lost at every size (0.48 ->
   // 0.41 of the copy peak back to back at 2^25)
@@ -1582,7 +1585,7 @@ reduce_kernel(RankPtrs in, Payload out, TileLoop T) {
     }
   };
   InPipe<C::kStagesR, C::kStageBytes, true, DYN> pipe{};
-  // the direct-scale variants (R = 3, 4) defer all but their first stage (see InPipe)
+  // the direct-scale variants (R = 2 - 4) defer all but their first stage (see InPipe)
   if constexpr (DYN) {
     const uint32_t ctr = ((smem_addr(smem_raw) + 127u) & ~127u) + (uint32_t)(C::kDynWarps * C::kRegion);
     dyn_counter_init(ctr);
