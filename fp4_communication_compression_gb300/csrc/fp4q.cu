@@ -1518,7 +1518,8 @@ struct ReduceCfg {
   static constexpr int kStagesR = R <= 4 ? 2 : 1;
   // launch bound (CTAs per SM): 5 where the kernel fits 96 registers without spilling its
   // running sum (R = 2: 21.6 -> 20.5 us, R = 8: 49.2 -> 47.1 us at 2^25 elements; R = 2 with
-  // the direct scales spills 8 bytes at G = 16 and is faster all the same); the R = 3, 4
+  // the direct scales spills 8 bytes at G = 16 and is faster all the same: at 4 CTAs, spill-
+  // free, 0.61 -> 0.60 of the copy peak back to back at 2^26, 0.66 -> 0.65 at 2^27); the R = 3, 4
   // variants prefetch every rank's scales into registers and keep 4 (at 5 they spill: R = 4
   // went from 29.4 to 36.8 us); R = 2 at 6 (80 registers, spilling) lost at every size (0.48 ->
   // 0.41 of the copy peak back to back at 2^25)
