@@ -92,6 +92,8 @@ constexpr int64_t kReduceDynTilesPerWarpR2 = 8;
 // elements) it still gains a little: launched back to back, compress 0.650 -> 0.655 of the
 // copy peak, roundtrip 0.636 -> 0.643, decompress-accumulate (beta = 1) 0.86 -> 0.90. For the
 // reduce below 384 tiles per SM it lost (R = 8 at 2^25: 47.2 -> 54.9 us).
+// 24 warps (80 registers, about 70 bytes of spill) lost: compress 0.83 -> 0.79 of the copy peak
+// at 2^29, 0.75 -> 0.72 at 2^27; roundtrip unchanged.
 constexpr int kCompressDynWarps = 20;
 // Decompress-accumulate into BF16 likewise (its 4 CTAs x 4 warps as one CTA). beta = 1:
 // 48.2 -> 47.0 us at 2^26, 96.2 -> 95.7 us at 2^27, equal at 2^28 - 2^29. beta = 0 (no
