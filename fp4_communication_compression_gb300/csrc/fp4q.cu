@@ -100,6 +100,9 @@ constexpr int kCompressDynWarps = 20;
 // destination pipeline; the warps claim from the counter directly): 0.72 -> 0.73 of the copy
 // peak at 2^26, 0.78 -> 0.81 at 2^27, 0.86 -> 0.89 at 2^29, within the timer's step at 2^25.
 constexpr int kDecompressDynWarps = 16;
+// beta = 0 has no destination stage, so its claiming CTA holds 20 warps (96 registers, no
+// spill): 0.81 -> 0.83 of the copy peak at 2^27, 0.89 -> 0.915 at 2^29, equal below.
+template <int BETA> constexpr int kDecDynWarps = BETA ? kDecompressDynWarps : 20;
 constexpr int64_t kCompressDynTilesPerWarp = 4;
 constexpr int kDynHeaderBytes = 2048;      // barriers of up to 31 warps, the claim counter last
 constexpr float kZeroLimit = 2688.0f * 0x1p-100f;   // all-zero block guard on A_b
@@ -1327,11 +1330,11 @@ compress_kernel(const __grid_constant__ CUtensorMap xmap, Payload P, TileLoop T)
 // K2: decompress-accumulate. payload -> dst (dtype DT), dst = BETA ? dst + x^ : x^.
 // The payload of the next tile is prefetched into registers; dst tiles are read (BETA) and
 // written through the swizzled shared staging buffer by TMA.
-// DYN (BF16 dst, BETA = 1): one CTA of kDecompressDynWarps warps per SM claiming its tiles
-// dynamically; the payload prefetch follows the claims (the tile claimed at the top of an
-// iteration is the one the refill loads next).
+// DYN (BF16 dst): one CTA of kDecDynWarps<BETA> warps per SM claiming its tiles dynamically;
+// the payload prefetch follows the claims (the tile claimed at the top of an iteration is the
+// one the refill loads next with BETA = 1, the one the next iteration decodes with BETA = 0).
 template <int G, int FWHT, int DT, int BETA, bool MX, bool DYN = false>
-__global__ void __launch_bounds__(DYN ? kDecompressDynWarps * 32 : kDecompressWarps * 32, DYN ? 1 : kDecompressCtas)
+__global__ void __launch_bounds__(DYN ? kDecDynWarps<BETA> * 32 : kDecompressWarps * 32, DYN ? 1 : kDecompressCtas)
 decompress_kernel(const __grid_constant__ CUtensorMap dmap, Payload P, TileLoop T) {
   static_assert(!DYN || DT == FP4Q_BF16, "dynamic claims: BF16 destinations");
   constexpr int TB = DT == FP4Q_BF16 ? 4096 : 8192;
@@ -2095,14 +2098,14 @@ fp4q_status launch_decompress(const Payload& P, int64_t n, void* dst, cudaStream
     fp4q_status st = FP4Q_OK;
     bool dyn = false;
     if constexpr (DT == FP4Q_BF16) {
-      dyn = sms > 0 && T.tiles >= kCompressDynTilesPerWarp * kDecompressDynWarps * sms;
+      dyn = sms > 0 && T.tiles >= kCompressDynTilesPerWarp * kDecDynWarps<B> * sms;
       if (dyn) {
         auto k = decompress_kernel<G, F, DT, B, MX, true>;
         Launch L;
-        st = plan(k, kDecompressDynWarps,
-                  WarpSmemLayout<kDecompressDynWarps, kDecompressStages, B ? TB : 0, kXBufBytes, kDynHeaderBytes>::kCtaBytes,
+        st = plan(k, kDecDynWarps<B>,
+                  WarpSmemLayout<kDecDynWarps<B>, kDecompressStages, B ? TB : 0, kXBufBytes, kDynHeaderBytes>::kCtaBytes,
                   T.tiles, L, 1);
-        if (st == FP4Q_OK) st = launch_pdl(k, L, kDecompressDynWarps * 32, s, dm, P, T);
+        if (st == FP4Q_OK) st = launch_pdl(k, L, kDecDynWarps<B> * 32, s, dm, P, T);
       }
     }
     if (!dyn) {
