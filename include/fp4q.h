@@ -101,6 +101,12 @@
  * kernel variant on a device sets that kernel's dynamic shared-memory limit and preferred
  * shared-memory carveout (the largest) and queries its occupancy; the results are cached per
  * kernel and device, and the library's own kernels are the only ones it configures.
+ * Calls may be captured in a CUDA graph once each kernel variant has run on the device (so
+ * that the first-call configuration above happens outside the capture): a launch carries
+ * everything it needs as kernel parameters (tensor maps of the given buffers included) and
+ * keeps no host state, so a replay on new contents of the same buffers computes what the
+ * same calls would. Several host threads may call the library at once, each on its own
+ * stream.
  */
 #ifndef FP4Q_H
 #define FP4Q_H
